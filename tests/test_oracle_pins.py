@@ -1,0 +1,287 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself
+(a library's independent routine for the number formats, closed forms, printed
+numbers from the pages, brute force on tiny inputs, special cases)."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tp_oracle as O
+
+
+def _load(d, name):
+    with open(os.path.join(d, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- formats
+
+
+def test_bf16_decode_all_patterns_match_float32_upper_half():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = O.bf16_bits_to_f64(bits)
+    finite = np.isfinite(ref)
+    assert np.array_equal(got[finite], ref[finite])
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    assert np.array_equal(np.isinf(got), np.isinf(ref))
+
+
+def test_bf16_decode_named_values():
+    cases = {0x3F80: 1.0, 0xBF80: -1.0, 0x4000: 2.0, 0x3F00: 0.5, 0x4049: 3.140625,
+             0x0080: 2.0 ** -126, 0x0001: 2.0 ** -133, 0x7F7F: (2 - 2 ** -7) * 2.0 ** 127}
+    for b, v in cases.items():
+        assert O.bf16_bits_to_f64(np.array([b], dtype=np.uint16))[0] == v
+
+
+def test_bf16_encode_matches_torch_cast_on_float32_values():
+    g = torch.Generator().manual_seed(5)
+    v = torch.randn(200000, generator=g) * torch.exp(torch.randn(200000, generator=g) * 20)
+    ref = v.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = O.f64_to_bf16_bits(v.numpy().astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_encode_ties_to_even():
+    one = 1.0
+    assert O.f64_to_bf16_bits(np.array([one + 2 ** -8]))[0] == 0x3F80          # tie -> even (1.0)
+    assert O.f64_to_bf16_bits(np.array([one + 3 * 2 ** -8]))[0] == 0x3F82      # tie -> even (1 + 2^-6)
+    assert O.f64_to_bf16_bits(np.array([one + 2 ** -8 + 2 ** -30]))[0] == 0x3F81  # above tie
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_bits_to_f64(codes)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin]) and np.array_equal(np.isnan(got), np.isnan(ref))
+    assert O.e4m3_bits_to_f64(np.array([0x7E], dtype=np.uint8))[0] == 448.0
+    assert O.e4m3_bits_to_f64(np.array([0x01], dtype=np.uint8))[0] == 2.0 ** -9
+    assert O.e4m3_bits_to_f64(np.array([0x38], dtype=np.uint8))[0] == 1.0
+
+
+def test_e4m3_encode_matches_torch_in_range_and_saturates():
+    g = torch.Generator().manual_seed(6)
+    v = (torch.rand(200000, generator=g) * 2 - 1) * 448
+    v = torch.cat([v, v * 1e-3, v * 1e-5, torch.tensor([0.0, -0.0, 448.0, -448.0])])
+    ref = v.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.f32_to_e4m3_bits_satfinite(v.numpy())
+    assert np.array_equal(got, ref)
+    sat = O.f32_to_e4m3_bits_satfinite(np.array([460.0, 1000.0, -1e30, np.inf], dtype=np.float32))
+    assert list(sat) == [0x7E, 0x7E, 0xFE, 0x7E]
+
+
+# ---------------------------------------------------------------- SwiGLU MLP
+
+
+def test_silu_closed_forms():
+    assert O.silu(0.0) == 0.0
+    assert abs(O.silu(50.0) - 50.0) < 1e-15
+    assert abs(O.silu(-50.0)) < 1e-18
+    z = np.linspace(-20, 20, 401)
+    # z*s(z) - (-z)*s(-z) = z*(s(z) + s(-z)) = z
+    assert np.allclose(O.silu(z) - O.silu(-z), z, rtol=0, atol=1e-13)
+    assert abs(O.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-16
+
+
+def test_mlp_hand_example(golden_dir):
+    g = _load(golden_dir, "mlp_hand_example.json")
+    y, h = O.mlp(np.array(g["x"]), np.array(g["w_gate"]), np.array(g["w_up"]),
+                 np.array(g["w_down"]), residual=np.array(g["x"]))
+    assert np.allclose(h, g["h"], atol=g["abs_tol"], rtol=0)
+    assert np.allclose(y, g["y"], atol=g["abs_tol"], rtol=0)
+
+
+def _brute_mlp(x, wg, wu, wd, res):
+    M, d = x.shape
+    F = wg.shape[1]
+    y = np.zeros((M, wd.shape[1]))
+    for m in range(M):
+        h = []
+        for j in range(F):
+            g = sum(x[m, k] * wg[k, j] for k in range(d))
+            u = sum(x[m, k] * wu[k, j] for k in range(d))
+            h.append(g / (1 + math.exp(-g)) * u)
+        for n in range(wd.shape[1]):
+            y[m, n] = res[m, n] + sum(h[j] * wd[j, n] for j in range(F))
+    return y
+
+
+def test_mlp_brute_force_non_square():
+    rng = np.random.default_rng(1)
+    M, d, F = 3, 5, 7
+    x, wg, wu = rng.normal(size=(M, d)), rng.normal(size=(d, F)), rng.normal(size=(d, F))
+    wd = rng.normal(size=(F, d))
+    y, _ = O.mlp(x, wg, wu, wd, residual=x)
+    assert np.allclose(y, _brute_mlp(x, wg, wu, wd, x), rtol=1e-12, atol=1e-12)
+
+
+def test_mlp_special_cases():
+    rng = np.random.default_rng(2)
+    x = rng.normal(size=(4, 16))
+    wg, wu, wd = rng.normal(size=(16, 32)), rng.normal(size=(16, 32)), rng.normal(size=(32, 16))
+    y, _ = O.mlp(x, wg, np.zeros_like(wu), wd, residual=x)
+    assert np.array_equal(y, x)                       # up = 0 -> h = 0
+    y, _ = O.mlp(x, np.zeros_like(wg), wu, wd, residual=x)
+    assert np.array_equal(y, x)                       # silu(0) = 0
+    y1, _ = O.mlp(x, wg, wu, wd)
+    y2, _ = O.mlp(x, wg, wu, 2 * wd)
+    assert np.allclose(y2, 2 * y1, rtol=1e-13, atol=1e-13)   # linear in the row-parallel matrix
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_sharded_equals_unsharded(t):
+    """Column split of A and row split of B, summed over shards, is the unsharded MLP."""
+    rng = np.random.default_rng(3)
+    x = rng.normal(size=(5, 24))
+    wg, wu, wd = rng.normal(size=(24, 64)), rng.normal(size=(24, 64)), rng.normal(size=(64, 24))
+    y, _ = O.mlp(x, wg, wu, wd, residual=x)
+    assert np.allclose(O.sharded_mlp(x, wg, wu, wd, t, residual=x), y, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- attention sub-block
+
+
+def test_attention_one_token_groups():
+    # n_q 4, n_kv 2, hd 1: q heads 0,1 -> kv 0; q heads 2,3 -> kv 1
+    qkv = np.array([[1, 2, 3, 4, 5, 6, 10, 20]], dtype=np.float64)
+    assert list(O.attention_one_token(qkv, 4, 2, 1)[0]) == [10, 10, 20, 20]
+
+
+@pytest.mark.parametrize("t", [1, 2, 4])
+def test_proj_sharded_heads_equal_unsharded(t):
+    """QKV column shards give each shard whole heads (its q heads and their kv heads);
+    local attention then row-parallel o_proj, summed over shards, is the unsharded block."""
+    rng = np.random.default_rng(4)
+    d, n_q, n_kv, hd, M = 32, 8, 4, 4, 3
+    x = rng.normal(size=(M, d))
+    wqkv = rng.normal(size=(d, (n_q + 2 * n_kv) * hd))
+    wo = rng.normal(size=(n_q * hd, d))
+    y, qkv = O.proj(x, wqkv, wo, n_q, n_kv, hd, residual=x)
+    qkv_sh = O.pack_colpar([wqkv], "qkv", t, n_q=n_q, n_kv=n_kv, hd=hd)
+    o_sh = O.pack_rowpar(wo, t)
+    z = x.copy()
+    for s in range(t):
+        q_s = x @ qkv_sh[s].T                          # [M, Q_s]: [q heads | k heads | v heads] of shard s
+        o_in_s = O.attention_one_token(q_s, n_q // t, n_kv // t, hd)
+        z = z + o_in_s @ o_sh[s].T
+    assert np.allclose(z, y, rtol=1e-12, atol=1e-12)
+
+
+def test_rmsnorm_closed_forms():
+    x = np.array([[3.0, 4.0]])
+    eps = 1e-5
+    assert np.allclose(O.rmsnorm(x, eps), x / math.sqrt(12.5 + eps), rtol=1e-15)
+    c = np.full((1, 64), -2.0)
+    assert np.allclose(O.rmsnorm(c, eps), -2.0 / math.sqrt(4.0 + eps), rtol=1e-15)
+    assert np.array_equal(O.rmsnorm(np.zeros((1, 8)), eps), np.zeros((1, 8)))
+
+
+# ---------------------------------------------------------------- shard layouts
+
+
+def test_gate_up_pack_layout_by_hand():
+    d, ffn, t = 2, 32, 2
+    wg = np.arange(d * ffn).reshape(d, ffn).astype(np.int64)
+    wu = 1000 + wg
+    sh = O.pack_colpar([wg, wu], "gate_up", t, ffn=ffn)
+    assert [a.shape for a in sh] == [(32, 2), (32, 2)]
+    # shard 0: gate 0-7, up 0-7, gate 8-15, up 8-15; shard 1 the same from column 16
+    expect0 = list(range(0, 8)) + [1000 + c for c in range(0, 8)] + list(range(8, 16)) + \
+        [1000 + c for c in range(8, 16)]
+    assert list(sh[0][:, 0]) == expect0
+    assert list(sh[1][:, 0]) == [v + 16 for v in expect0]
+    assert list(sh[1][:, 1]) == [v + 16 + ffn for v in expect0]   # row k=1 of W is +ffn
+
+
+def test_qkv_pack_layout_by_hand():
+    d, n_q, n_kv, hd, t = 1, 4, 2, 2, 2
+    w = np.arange((n_q + 2 * n_kv) * hd).reshape(1, -1)   # column index == value
+    sh = O.pack_colpar([w], "qkv", t, n_q=n_q, n_kv=n_kv, hd=hd)
+    # q heads {0,1} (cols 0-3), k head 0 (cols 8-9), v head 0 (cols 12-13)
+    assert list(sh[0][:, 0]) == [0, 1, 2, 3, 8, 9, 12, 13]
+    assert list(sh[1][:, 0]) == [4, 5, 6, 7, 10, 11, 14, 15]
+
+
+def test_rowpar_pack_layout_and_bytes():
+    w = np.arange(8 * 3).reshape(8, 3)                     # [in=8, out=3]
+    sh = O.pack_rowpar(w, 4)
+    assert sh[1].shape == (3, 2) and list(sh[1][0]) == [w[2, 0], w[3, 0]]
+    assert sum(a.size for a in sh) == w.size              # per-shard bytes are 1/t of the total
+
+
+def test_per_shard_bytes_are_one_over_t():
+    for t in (1, 2, 4, 8):
+        wg = np.zeros((64, 128), dtype=np.uint16)
+        sh = O.pack_colpar([wg, wg], "gate_up", t, ffn=128)
+        assert all(a.size * t == 2 * wg.size for a in sh)
+
+
+# ---------------------------------------------------------------- FP8 weights
+
+
+def test_fp8_quantizer_properties():
+    rng = np.random.default_rng(7)
+    w = (rng.normal(size=(64, 40)) * 0.02).astype(np.float32)
+    w[:, 3] = 0.0
+    q, s = O.quantize_fp8_per_channel(w)
+    assert s[3] == 1.0 and np.all(q[:, 3] == 0)
+    deq = O.dequantize_fp8(q, s)
+    # each column's absmax lands on +-448 (code 0x7E / 0xFE)
+    amax_rows = np.argmax(np.abs(w), axis=0)
+    for n in range(40):
+        if n != 3:
+            assert q[amax_rows[n], n] & 0x7F == 0x7E
+    # round to nearest with 3 mantissa bits: error <= 2^-4 relative, or half a subnormal step
+    err = np.abs(deq - w.astype(np.float64))
+    bound = np.maximum(np.abs(w) * 2.0 ** -4, s[None, :].astype(np.float64) * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(err <= bound)
+
+
+def test_fp8_exact_values_round_trip():
+    # a column whose entries are e4m3 values times a power of two scale round-trips exactly
+    vals = np.array([448, 1, -0.5, 0.015625, 2 ** -9, 96, -448, 0], dtype=np.float32)
+    w = np.stack([vals * 2.0 ** -10, vals], axis=1).astype(np.float32)
+    q, s = O.quantize_fp8_per_channel(w)
+    assert np.array_equal(O.dequantize_fp8(q, s), w.astype(np.float64))
+
+
+# ---------------------------------------------------------------- accounting printed on the pages
+
+
+def test_accounting_matches_printed_numbers(golden_dir):
+    g = _load(golden_dir, "accounting.json")
+    m70, m405 = g["models"]["llama31_70b"], g["models"]["llama31_405b"]
+
+    def full_params(m):
+        lin = O.layer_linear_params(m["d"], m["ffn"], m["n_q"], m["n_kv"], m["hd"])
+        return m["n_layers"] * lin + 2 * m["vocab"] * m["d"]
+
+    shp = {k: m70[k] for k in ("d", "ffn", "n_q", "n_kv", "hd")}
+    got = {
+        "decode_bytes_per_gpu_70b_tp8_bf16": O.decode_bytes_per_shard(
+            **shp, n_layers=m70["n_layers"], vocab=m70["vocab"], t=8, bytes_per_param=2),
+        "weights_70b_bf16_unsharded": full_params(m70) * 2,
+        "allreduce_bytes_per_token_70b_bf16": O.allreduce_bytes_per_token(m70["d"], 2),
+        "allreduces_per_token_70b": O.allreduces_per_token(m70["n_layers"]),
+        "reduced_bytes_per_token_70b": O.allreduces_per_token(m70["n_layers"]) *
+        O.allreduce_bytes_per_token(m70["d"], 2),
+        "prefill_flops_70b_4096": O.forward_flops(full_params(m70), 4096),
+        "weights_405b_bf16": full_params(m405) * 2,
+        "weights_405b_fp8": full_params(m405) * 1,
+        "weights_per_gpu_405b_fp8_tp8": full_params(m405) * 1 / 8,
+    }
+    for e in g["printed"]:
+        v = got[e["name"]]
+        assert abs(v - e["value"]) <= e["rel_tol"] * e["value"] + 1e-9, (e["name"], v, e["value"])
+
+
+def test_metrics():
+    y = np.array([[3.0, 4.0]])
+    assert O.rel_frobenius(y, y) == 0.0
+    assert abs(O.rel_frobenius(y * 1.01, y) - 0.01) < 1e-12
+    assert abs(O.max_err_over_rms(y + np.array([[0.0, 0.5]]), y) - 0.5 / math.sqrt(12.5)) < 1e-12
