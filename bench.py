@@ -1,0 +1,356 @@
+"""Benchmark: Llama-3-8B-shaped tensor-parallel MLP layer, decode, t=8 logical shards on one GPU.
+
+One step = one SwiGLU MLP forward (column-parallel gate/up + SwiGLU, row-parallel down +
+fixed-order shard fold + residual) for each decode batch M in {1, 8, 32, 64}: 105 tokens.
+Weights are 352 MB (> 129 MB L2), read once per forward, so no L2 flush is needed between
+forwards.  Prints one JSON line (see the fields below).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tpx|reference]
+
+--impl reference times the float64 CPU oracle on this host on a bounded sample of the same
+workload (there is no reference GPU implementation to run).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D, FFN, T = 4096, 14336, 8
+MS = (1, 8, 32, 64)
+METRIC = "decode tokens/s and HBM GB/s (% peak); prefill TFLOP/s (% peak) per TP layer"
+WORKLOAD = "llama3-8b MLP layer decode (d 4096, ffn 14336, t 8 logical shards), M in {1,8,32,64}"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return j["hbm_gbs"], "measured"
+    return 6800.0, "fallback"
+
+
+def weight_bytes():
+    return 3 * D * FFN * 2
+
+
+def colpar_bytes(M):     # gate/up weights + x in + h out
+    return 2 * D * FFN * 2 + M * D * 2 + M * FFN * 2
+
+
+def rowpar_bytes(M):     # down weights + h in + residual in + y out
+    return FFN * D * 2 + M * FFN * 2 + 2 * M * D * 2
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, path):
+        self.path, self.p = path, None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-i", os.environ.get("LOCAL_RANK", "0"), "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        t0 = time.time()          # wait for the first sample so the timed region is covered
+        while self.p and time.time() - t0 < 3.0:
+            if os.path.exists(self.path) and os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.05)
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            self.p.wait()
+            self.f.close()
+
+    def summary(self):
+        try:
+            rows = [l.split(",") for l in open(self.path).read().splitlines() if l.strip()]
+        except OSError:
+            rows = []
+        sm = [float(r[1]) for r in rows if len(r) >= 9 and r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) >= 9 and r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows if len(r) >= 9 for i in range(4)
+                          if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if os.environ.get("BENCH_BACKEND") != "gloo" else "gloo")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, dev):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_record():
+    """Per-launch DRAM traffic of the gate/up kernel from the committed ncu summary, if the
+    kernel source is unchanged since it was taken (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    src = os.path.join(ROOT, "megatron_tensor_transformer_gb300", "csrc", "skinny.cu")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    return rec if rec.get("skinny_cu_sha256") == h else None
+
+
+def oracle_sample(wg, wu, wd, seconds=10.0):
+    """CPU oracle on this host: the same four decode batches, repeated for about `seconds`."""
+    import numpy as np
+    from megatron_tensor_transformer_gb300 import inputs
+    from oracle import tp_oracle as O
+    xs = [O.as_f64(inputs.normal_bf16((M, D), 1.0, 0, inputs.STREAM_X, "cpu").view(
+        __import__("torch").int16).numpy().view(np.uint16)) for M in MS]
+    toks, t0, reps = 0, time.perf_counter(), 0
+    while True:
+        for x in xs:
+            O.mlp(x, wg, wu, wd, residual=x)
+            toks += x.shape[0]
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return toks / el, reps, el
+
+
+def host_weights():
+    """The benchmark's weights, drawn on the device, as float64 arrays for the oracle."""
+    import numpy as np
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs
+    from oracle import tp_oracle as O
+    dev = torch.device("cuda", torch.cuda.current_device()) if torch.cuda.is_available() else "cpu"
+    _, wg, wu, wd = inputs.mlp_inputs(D, FFN, 1, seed=0, device=dev)
+    f = lambda w: O.as_f64(w.cpu().view(torch.int16).numpy().view(np.uint16))
+    return f(wg), f(wu), f(wd)
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wg, wu, wd = host_weights()
+    for _ in range(args.warmup):
+        oracle_sample(wg, wu, wd, seconds=0.0)
+    t0 = time.perf_counter()
+    toks = 0
+    for _ in range(args.steps):
+        v, reps, el = oracle_sample(wg, wu, wd, seconds=0.0)
+        toks += sum(MS) * reps
+    el = time.perf_counter() - t0
+    value = toks / el
+    sample = "one step = the four decode batches M=1,8,32,64 of the 8B MLP, float64, unsharded"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "tokens_per_step": sum(MS)},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_tpx(args, rank, world, local):
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    tpx.lib()
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wg, wu, wd = host_weights()
+        v, reps, el = oracle_sample(wg, wu, wd, seconds=args.cpu_seconds)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"{reps} repetitions of the four decode batches M=1,8,32,64 (float64, unsharded "
+                         f"8B MLP incl. residual) in {el:.1f} s"}
+        del wg, wu, wd
+
+    _, wg, wu, wd = inputs.mlp_inputs(D, FFN, 1, seed=0, device=dev)
+    sh = tpx.make_shape(D, ffn=FFN, t=T)
+    stream = torch.cuda.Stream(device=dev)
+    gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu, stream=stream)
+    dn_w, dn = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, wd, stream=stream)
+    stream.synchronize()
+    del wg, wu, wd
+    xs = {M: inputs.normal_bf16((M, D), 1.0, 0, inputs.STREAM_X, dev) for M in MS}
+    hs = {M: torch.empty((M, FFN), dtype=torch.bfloat16, device=dev) for M in MS}
+    ys = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
+    ws = tpx.new_workspace(sh, max(MS), dev)
+    K = args.steps
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in MS] for _ in range(K)]
+
+    def step(i=None):
+        for j, M in enumerate(MS):
+            if i is not None:
+                ev[i][j][0].record(stream)
+            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], stream=stream)
+            if i is not None:
+                ev[i][j][1].record(stream)
+            tpx.tp_rowpar_forward(dn, dn_w, hs[M], xs[M], ys[M], ws, stream=stream)
+            if i is not None:
+                ev[i][j][2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        barrier(world)
+        torch.cuda.synchronize()
+        t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = tpx.tp_launch_count()
+        with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_rank{rank}.csv") if os.path.isdir(
+                os.path.join(ROOT, "gpurun_out")) else f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
+            t_start.record(stream)
+            for i in range(K):
+                step(i)
+            t_end.record(stream)
+            t_end.synchronize()
+        launches = tpx.tp_launch_count() - n0
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = t_start.elapsed_time(t_end)
+    ms_max = max_over_ranks(ms, world, dev)
+    per_M = {}
+    col_t = col_b = 0.0
+    for j, M in enumerate(MS):
+        c = sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K)) / K
+        r = sum(ev[i][j][1].elapsed_time(ev[i][j][2]) for i in range(K)) / K
+        col_t += c
+        col_b += colpar_bytes(M)
+        per_M[str(M)] = {"tokens_per_s": M / ((c + r) * 1e-3), "colpar_us": 1e3 * c, "rowpar_us": 1e3 * r,
+                         "colpar_gbs": colpar_bytes(M) / (c * 1e-3) / 1e9,
+                         "rowpar_gbs": rowpar_bytes(M) / (r * 1e-3) / 1e9,
+                         "layer_gbs": (colpar_bytes(M) + rowpar_bytes(M)) / ((c + r) * 1e-3) / 1e9}
+    peak, peak_kind = peaks()
+    achieved = col_b / (col_t * 1e-3) / 1e9
+    tr = traffic_record()
+    e2e = run_e2e(args, gu, gu_w, dn, dn_w, sh, dev)
+    tokens = sum(MS) * K * world
+    step_bytes = sum(colpar_bytes(M) + rowpar_bytes(M) for M in MS)
+    out = {
+        "metric": METRIC, "value": tokens / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "d": D, "ffn": FFN, "t": T, "M": list(MS),
+                   "tokens_per_step": sum(MS), "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "weights 352 MB per forward > 129 MB L2; no flush"},
+        "hbm_gbs_step": step_bytes / (ms_max / K * 1e-3) / 1e9,
+        "hbm_frac_step": step_bytes / (ms_max / K * 1e-3) / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": "colpar_kernel (gate/up + SwiGLU)", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind + " (hbm_gbs, burst)", "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": None if tr is None else tr.get("bytes_per_launch_M64")},
+        "per_M": per_M,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+def run_e2e(args, gu, gu_w, dn, dn_w, sh, dev):
+    """Through the public C-ABI call tp_mlp_forward with HOST buffers: every step copies each
+    batch's x from pinned host memory, runs the block, and copies y back."""
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+    stream = torch.cuda.Stream(device=dev)
+    hx = {M: inputs.normal_bf16((M, D), 1.0, 0, inputs.STREAM_X, "cpu").pin_memory() for M in MS}
+    hy = {M: torch.empty((M, D), dtype=torch.bfloat16).pin_memory() for M in MS}
+    dx = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
+    dy = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
+    dh = {M: torch.empty((M, FFN), dtype=torch.bfloat16, device=dev) for M in MS}
+    ws = tpx.new_workspace(sh, max(MS), dev)
+
+    def step():
+        for M in MS:
+            dx[M].copy_(hx[M], non_blocking=True)
+            tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, dx[M], dx[M], dy[M], dh[M], ws, stream=stream)
+            hy[M].copy_(dy[M], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        b.synchronize()
+    ms = a.elapsed_time(b)
+    nbytes = sum(M * D * 2 for M in MS)
+    return {"value": sum(MS) * args.steps / (ms * 1e-3), "unit": "tokens/s",
+            "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="tpx", choices=["tpx", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_tpx(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * tpx.h -- C ABI of libtpx.so: Megatron-style tensor-parallel linear layers of a
+ * Llama-style block, all t logical shards on one GB300 (sm_103a).
+ *
+ * The method ("The Tensor-Parallel Shard Group", scalablesystem.dev; "Tensor
+ * Parallelism (Megatron-Style)", arunshar.com ch. 12; "Step 1: tensor parallelism
+ * slices every layer", vidyal.ai model-parallelism):
+ *   - the first linear of a block is split along its OUTPUT dim (column-parallel):
+ *     shard s owns a slice of output features, needs no communication in, and
+ *     applies the nonlinearity to its own slice;
+ *   - the second linear is split along its INPUT dim (row-parallel): shard s
+ *     produces a partial Z_s of the full output and Z = sum_s Z_s ("all-reduce").
+ * Here the sum over shards is a deterministic fixed-order fp32 fold on the device:
+ *     y = bf16_rne( (((Z_0 + Z_1) + Z_2) + ... + Z_{t-1}) + float(residual) ).
+ *
+ * Conventions for every entry point below:
+ *   - Pointers are DEVICE pointers unless marked (host).  All buffers are owned by
+ *     the caller; the library never allocates and never synchronises on the forward
+ *     path.  Work is enqueued on `stream` (a cudaStream_t passed as void*, NULL =
+ *     legacy default stream).
+ *   - Matrices are row-major.  Activations are bf16 [M, features].  Unsharded
+ *     weights are bf16 in the [in, out] orientation of Y = X A.
+ *   - Every argument check runs on the host BEFORE any launch and returns a status;
+ *     a failed check enqueues nothing.  Launch errors return TP_ERR_CUDA.
+ *   - Device pointers must be 16-byte aligned (TP_ERR_ALIGN otherwise).
+ *   - Not thread-safe per stream: calls that share a workspace must be ordered.
+ */
+#ifndef TPX_H
+#define TPX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1,     /* NULL pointer, M < 0, unknown kind/flags */
+  TP_ERR_SHAPE = 2,           /* t not in {1,2,4,8}, t does not divide ffn / n_kv / n_q, ... */
+  TP_ERR_ALIGN = 3,           /* pointer not 16-byte aligned, or a dim not a multiple the kernels need */
+  TP_ERR_LAYOUT_MISMATCH = 4, /* packed descriptor does not match the call (wrong shard layout) */
+  TP_ERR_WORKSPACE = 5,       /* workspace NULL or smaller than tp_workspace_bytes() */
+  TP_ERR_CUDA = 6,            /* a CUDA runtime call or launch failed */
+  TP_ERR_TIMEOUT = 7,         /* tp_sync deadline passed with work still pending */
+  TP_ERR_DEVICE_TIMEOUT = 8,  /* a bounded device-side wait gave up (device error word set) */
+  TP_ERR_UNSUPPORTED = 9      /* a valid request this build does not implement */
+} tp_status;
+
+typedef enum { TP_BF16 = 0, TP_FP8_E4M3 = 1 } tp_wtype;
+
+/* Which weight of the block a packed buffer holds. */
+typedef enum {
+  TP_W_GATE_UP = 0, /* column-parallel W_gate and W_up, [d, ffn] each */
+  TP_W_DOWN = 1,    /* row-parallel W_down, [ffn, d] */
+  TP_W_QKV = 2,     /* column-parallel W_qkv, [d, (n_q + 2 n_kv) * head_dim] */
+  TP_W_O = 3        /* row-parallel W_o, [n_q * head_dim, d] */
+} tp_wkind;
+
+/* Model dims and the shard count.  ffn is used by GATE_UP/DOWN, the head dims by
+ * QKV/O.  t must be 1, 2, 4 or 8 and divide ffn, n_q and n_kv ("TP degree must
+ * divide the KV heads"; t > n_kv head replication is not supported). */
+typedef struct {
+  int32_t d, ffn, n_q_heads, n_kv_heads, head_dim, t;
+  int32_t wtype; /* tp_wtype */
+} tp_shape;
+
+#define TP_DESC_MAGIC 0x54505831u /* "TPX1" */
+#define TP_LAYOUT_VERSION 1u
+
+/* Host struct describing a packed weight buffer.  Shard s starts at byte
+ * s * shard_stride_bytes and holds a K-major matrix [rows_per_shard, k_per_shard]
+ * (one row per output feature, the nn.Linear [out, in] orientation) of bf16 or
+ * e4m3 codes; for FP8, float32 scales follow at scales_offset within the shard
+ * (one per row of the shard).  Packed-row order:
+ *   GATE_UP: shard s holds gate/up columns [s*F_s, (s+1)*F_s), F_s = ffn/t,
+ *            interleaved in blocks of 8 features: rows 16b..16b+7 = gate columns
+ *            s*F_s+8b+0..7, rows 16b+8..16b+15 = up columns s*F_s+8b+0..7.
+ *   QKV:     shard s holds its q heads [s*n_q/t, (s+1)*n_q/t), then its kv heads
+ *            [s*n_kv/t, (s+1)*n_kv/t) of k, then the same of v (head_dim rows each);
+ *            q head h uses kv head h / (n_q/n_kv), so a GQA group never straddles shards.
+ *   DOWN/O:  shard s holds rows [s*K_s, (s+1)*K_s) of the [in, out] weight,
+ *            transposed: element [n][k] = W[s*K_s + k][n]; FP8 scales replicated.
+ * FP8: s_n = absmax over the whole unsharded input dim of column n / 448 (fp32),
+ * 1 for an all-zero column; code = e4m3 RNE satfinite(W / s_n) (fp32 divide). */
+typedef struct {
+  uint32_t magic, layout_version;
+  int32_t kind, wtype;
+  tp_shape shape;
+  int64_t rows_per_shard, k_per_shard;
+  uint64_t shard_payload_bytes, scales_offset, shard_stride_bytes, total_bytes;
+} tp_packed_desc;
+
+/* Flags */
+#define TP_F_UNFUSED_REDUCE 0x1u  /* row-parallel: write shard partials to the workspace, then
+                                     run tp_reduce_partials (same bits as the fused path) */
+#define TP_F_FP32_COLPAR_OUT 0x2u /* tp_colpar_forward: write fp32 instead of bf16 */
+
+/* Size in bytes of the packed buffer for (shape, kind); 0 if the shape is invalid. */
+size_t tp_packed_bytes(const tp_shape* shape /* host */, int32_t kind);
+
+/* Fill *desc (host) for (shape, kind) without touching the device. */
+tp_status tp_describe(const tp_shape* shape /* host */, int32_t kind, tp_packed_desc* desc /* host */);
+
+/* Split and pack an unsharded weight for degree t (column split on the output dim for
+ * GATE_UP/QKV, row split on the input dim for DOWN/O; "ColumnParallelLinear" /
+ * "RowParallelLinear", scalablesystem.dev).  W0: [in,out] bf16 (W_gate for GATE_UP);
+ * W1: W_up for GATE_UP, else NULL.  packed: packed_bytes >= tp_packed_bytes().
+ * Writes the layout described above; for FP8 also quantises (shape.wtype).  Fills
+ * *desc_out (host).  Stream-ordered; W0/W1 may be freed after the stream reaches it. */
+tp_status tp_partition_weights(const tp_shape* shape /* host */, int32_t kind, const void* W0,
+                               const void* W1, void* packed, size_t packed_bytes,
+                               tp_packed_desc* desc_out /* host */, void* stream);
+
+/* Workspace bytes the forward calls need for M tokens (shard partials and tickets).
+ * The workspace must be zero-filled once before first use; calls leave it reusable. */
+size_t tp_workspace_bytes(const tp_shape* shape /* host */, int32_t M, uint32_t flags);
+
+/* SwiGLU MLP block: h = silu(x Wg) * (x Wu) column-parallel per shard, then
+ * y = fold_s(h_s Wd_s) + residual row-parallel ("gate_proj and up_proj are
+ * column-parallel ... down_proj is row-parallel", scalablesystem.dev).
+ * x, residual (nullable): [M, d] bf16; y: [M, d] bf16; h_out: [M, ffn] bf16 scratch for
+ * h, required (it is the activation between the two halves, shard s owns columns
+ * [s*F_s, (s+1)*F_s)).  M == 0 returns TP_OK with no work.  y may alias residual. */
+tp_status tp_mlp_forward(const tp_packed_desc* gu /* host */, const void* gu_w,
+                         const tp_packed_desc* dn /* host */, const void* dn_w, const void* x,
+                         const void* residual, int32_t M, void* y, void* h_out, void* ws,
+                         size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Attention sub-block: qkv = x Wqkv column-parallel (each shard owns whole heads);
+ * o_in = local attention per shard; y = fold_s(o_in_s Wo_s) + residual row-parallel
+ * ("TPAttentionBlock", scalablesystem.dev).  The attention core is a one-token
+ * context: every q head returns the v of its kv group.  qkv_out: [M, (n_q+2n_kv)hd]
+ * bf16, shard-major (shard s = [q_s | k_s | v_s]); o_in: [M, n_q*hd] bf16 scratch. */
+tp_status tp_proj_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
+                          const tp_packed_desc* o /* host */, const void* o_w, const void* x,
+                          const void* residual, int32_t M, void* y, void* qkv_out, void* o_in,
+                          void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* The "all-reduce" on one GPU: y[m][n] = bf16_rne(((P_0 + P_1) + ... + P_{t-1})[m][n]
+ * + float(residual[m][n])), a left fold in shard order (Z = sum_k Z_k, arunshar.com;
+ * summation order fixed so results are reproducible).  partials: [t][M][d] fp32;
+ * residual nullable [M, d] bf16; y [M, d] bf16. */
+tp_status tp_reduce_partials(const float* partials, int32_t t, int32_t M, int32_t d,
+                             const void* residual, void* y, void* stream);
+
+/* Column-parallel building block: out[m][s*rows + r] for every shard s and packed row r.
+ * GATE_UP: out = h [M, ffn] bf16 (SwiGLU applied);  QKV: out = qkv [M, Q] bf16.
+ * With TP_F_FP32_COLPAR_OUT (QKV only) out is fp32. */
+tp_status tp_colpar_forward(const tp_packed_desc* desc /* host */, const void* w, const void* x,
+                            int32_t M, void* out, uint32_t flags, void* stream);
+
+/* Row-parallel building block without the fold: partials[s][m][n] = (a_s W_s)[m][n],
+ * a_s = columns [s*K_s, (s+1)*K_s) of a [M, t*K_s] bf16; partials [t][M][N] fp32. */
+tp_status tp_rowpar_partials(const tp_packed_desc* desc /* host */, const void* w, const void* a,
+                             int32_t M, float* partials, void* stream);
+
+/* Row-parallel linear with its "all-reduce" ("RowParallelLinear.forward", scalablesystem.dev):
+ * y[m][n] = bf16(fold_s (a_s W_s)[m][n] + residual[m][n]) for DOWN or O weights, a: [M, t*K_s]
+ * bf16, residual nullable [M, N], y [M, N].  Same kernels and bits as the second half of
+ * tp_mlp_forward / tp_proj_forward; ws as for those (tp_workspace_bytes). */
+tp_status tp_rowpar_forward(const tp_packed_desc* desc /* host */, const void* w, const void* a,
+                            const void* residual, int32_t M, void* y, void* ws, size_t ws_bytes,
+                            uint32_t flags, void* stream);
+
+/* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g). */
+tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,
+                     void* stream);
+
+/* Block until `stream` drains or timeout_ms passes (TP_ERR_TIMEOUT; the work keeps
+ * running).  Also reports a device error word set by a bounded device-side wait
+ * (TP_ERR_DEVICE_TIMEOUT) and clears it. */
+tp_status tp_sync(void* stream, int32_t timeout_ms);
+
+/* Static string for a status code. */
+const char* tp_status_str(tp_status s);
+
+/* Number of kernel launches this library has enqueued since load (for launch counting). */
+uint64_t tp_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TPX_H */

@@ -1,0 +1,424 @@
+// C ABI of libtpx.so: argument checks, packed-weight descriptors, kernel dispatch.
+// Every check runs on the host before anything is enqueued.
+#include <atomic>
+#include <chrono>
+#include <cstring>
+#include <thread>
+
+#include "common.cuh"
+#include "pack.h"
+#include "skinny.h"
+#include "small.h"
+
+namespace tpx {
+static std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+}  // namespace tpx
+
+using namespace tpx;
+
+namespace {
+
+constexpr uint64_t kAlign = 256;
+inline uint64_t align_up(uint64_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+inline cudaStream_t S(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// k per chunk of the decode kernels: 32 bf16 or 64 e4m3 values (16 bytes per thread per row)
+inline int k_chunk(int wtype) { return wtype == TP_FP8_E4M3 ? 64 : 32; }
+
+tp_status check_shape(const tp_shape* sh, int kind) {
+  if (!sh) return TP_ERR_INVALID_ARG;
+  if (kind < TP_W_GATE_UP || kind > TP_W_O) return TP_ERR_INVALID_ARG;
+  if (sh->wtype != TP_BF16 && sh->wtype != TP_FP8_E4M3) return TP_ERR_INVALID_ARG;
+  const int t = sh->t;
+  if (t != 1 && t != 2 && t != 4 && t != 8) return TP_ERR_SHAPE;
+  if (sh->d <= 0) return TP_ERR_SHAPE;
+  if (sh->d % 32) return TP_ERR_ALIGN;
+  const int kc = k_chunk(sh->wtype);
+  if (kind == TP_W_GATE_UP || kind == TP_W_DOWN) {
+    if (sh->ffn <= 0 || sh->ffn % t) return TP_ERR_SHAPE;
+    const int fs = sh->ffn / t;
+    if (fs % 8) return TP_ERR_ALIGN;                       // gate/up interleave blocks of 8
+    if (kind == TP_W_GATE_UP && sh->d % kc) return TP_ERR_ALIGN;
+    if (kind == TP_W_DOWN && fs % kc) return TP_ERR_ALIGN;
+  } else {
+    const int nq = sh->n_q_heads, nkv = sh->n_kv_heads, hd = sh->head_dim;
+    if (nq <= 0 || nkv <= 0 || hd <= 0) return TP_ERR_SHAPE;
+    if (nq % nkv) return TP_ERR_SHAPE;                      // GQA groups
+    if (nq % t || nkv % t) return TP_ERR_SHAPE;             // t divides the q and kv heads
+    if (hd % 8) return TP_ERR_ALIGN;
+    if (kind == TP_W_QKV && sh->d % kc) return TP_ERR_ALIGN;
+    if (kind == TP_W_O && (nq / t * hd) % kc) return TP_ERR_ALIGN;
+  }
+  return TP_OK;
+}
+
+void geometry(const tp_shape* sh, int kind, int64_t* rows, int64_t* K, int64_t* out_cols) {
+  const int t = sh->t;
+  switch (kind) {
+    case TP_W_GATE_UP: *rows = 2LL * sh->ffn / t; *K = sh->d; *out_cols = sh->ffn; break;
+    case TP_W_DOWN: *rows = sh->d; *K = sh->ffn / t; *out_cols = sh->d; break;
+    case TP_W_QKV:
+      *rows = (int64_t)(sh->n_q_heads + 2 * sh->n_kv_heads) / t * sh->head_dim;
+      *K = sh->d;
+      *out_cols = (int64_t)(sh->n_q_heads + 2 * sh->n_kv_heads) * sh->head_dim;
+      break;
+    default:
+      *rows = sh->d; *K = (int64_t)sh->n_q_heads / t * sh->head_dim; *out_cols = sh->d; break;
+  }
+}
+
+tp_status check_desc(const tp_packed_desc* d, int kind, const void* w) {
+  if (!d || !w) return TP_ERR_INVALID_ARG;
+  if (!aligned16(w)) return TP_ERR_ALIGN;
+  if (d->magic != TP_DESC_MAGIC || d->layout_version != TP_LAYOUT_VERSION) return TP_ERR_LAYOUT_MISMATCH;
+  if (d->kind != kind) return TP_ERR_LAYOUT_MISMATCH;
+  tp_packed_desc ref;
+  if (tp_describe(&d->shape, kind, &ref) != TP_OK) return TP_ERR_LAYOUT_MISMATCH;
+  if (ref.rows_per_shard != d->rows_per_shard || ref.k_per_shard != d->k_per_shard ||
+      ref.shard_payload_bytes != d->shard_payload_bytes || ref.scales_offset != d->scales_offset ||
+      ref.shard_stride_bytes != d->shard_stride_bytes || ref.total_bytes != d->total_bytes ||
+      ref.wtype != d->wtype)
+    return TP_ERR_LAYOUT_MISMATCH;
+  return TP_OK;
+}
+
+tp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TP_OK : TP_ERR_CUDA; }
+
+// Workspace: shard partials of one token block [t][min(M,64)][N] fp32, then row-tile tickets.
+uint64_t partials_bytes(int t, int M, int N) {
+  const int mb = M < kSkinnyMaxM ? M : kSkinnyMaxM;
+  return align_up((uint64_t)t * mb * N * 4);
+}
+uint64_t ticket_bytes(int N) { return align_up((uint64_t)(N / 8 + 1) * 4); }
+
+}  // namespace
+
+extern "C" {
+
+const char* tp_status_str(tp_status s) {
+  switch (s) {
+    case TP_OK: return "TP_OK";
+    case TP_ERR_INVALID_ARG: return "TP_ERR_INVALID_ARG";
+    case TP_ERR_SHAPE: return "TP_ERR_SHAPE";
+    case TP_ERR_ALIGN: return "TP_ERR_ALIGN";
+    case TP_ERR_LAYOUT_MISMATCH: return "TP_ERR_LAYOUT_MISMATCH";
+    case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE";
+    case TP_ERR_CUDA: return "TP_ERR_CUDA";
+    case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    case TP_ERR_DEVICE_TIMEOUT: return "TP_ERR_DEVICE_TIMEOUT";
+    case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
+  }
+  return "TP_ERR_UNKNOWN";
+}
+
+uint64_t tp_launch_count(void) { return g_launches.load(); }
+
+tp_status tp_describe(const tp_shape* shape, int32_t kind, tp_packed_desc* desc) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  tp_status st = check_shape(shape, kind);
+  if (st != TP_OK) return st;
+  memset(desc, 0, sizeof(*desc));
+  desc->magic = TP_DESC_MAGIC;
+  desc->layout_version = TP_LAYOUT_VERSION;
+  desc->kind = kind;
+  desc->wtype = shape->wtype;
+  desc->shape = *shape;
+  int64_t rows, K, oc;
+  geometry(shape, kind, &rows, &K, &oc);
+  desc->rows_per_shard = rows;
+  desc->k_per_shard = K;
+  const bool fp8 = shape->wtype == TP_FP8_E4M3;
+  desc->shard_payload_bytes = (uint64_t)rows * K * (fp8 ? 1 : 2);
+  desc->scales_offset = fp8 ? align_up(desc->shard_payload_bytes) : desc->shard_payload_bytes;
+  desc->shard_stride_bytes = align_up(desc->scales_offset + (fp8 ? (uint64_t)rows * 4 : 0));
+  desc->total_bytes = desc->shard_stride_bytes * shape->t;
+  return TP_OK;
+}
+
+size_t tp_packed_bytes(const tp_shape* shape, int32_t kind) {
+  tp_packed_desc d;
+  return tp_describe(shape, kind, &d) == TP_OK ? (size_t)d.total_bytes : 0;
+}
+
+tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* W0, const void* W1,
+                               void* packed, size_t packed_bytes, tp_packed_desc* desc_out,
+                               void* stream) {
+  tp_packed_desc d;
+  tp_status st = tp_describe(shape, kind, &d);
+  if (st != TP_OK) return st;
+  if (!W0 || !packed || !desc_out) return TP_ERR_INVALID_ARG;
+  if ((kind == TP_W_GATE_UP) != (W1 != nullptr)) return TP_ERR_INVALID_ARG;
+  if (!aligned16(W0) || (W1 && !aligned16(W1)) || !aligned16(packed)) return TP_ERR_ALIGN;
+  if (packed_bytes < d.total_bytes) return TP_ERR_INVALID_ARG;
+  PackGeom g{};
+  g.kind = kind;
+  g.colpar = kind == TP_W_GATE_UP || kind == TP_W_QKV;
+  g.fp8 = shape->wtype == TP_FP8_E4M3;
+  g.t = shape->t;
+  int64_t rows, K, oc;
+  geometry(shape, kind, &rows, &K, &oc);
+  g.rows = (int)rows;
+  g.K = (int)K;
+  g.out_cols = (int)oc;
+  g.ffn = shape->ffn;
+  g.n_q = shape->n_q_heads;
+  g.n_kv = shape->n_kv_heads;
+  g.hd = shape->head_dim;
+  g.W0 = static_cast<const uint16_t*>(W0);
+  g.W1 = static_cast<const uint16_t*>(W1);
+  g.shard_stride = d.shard_stride_bytes;
+  g.scales_offset = d.scales_offset;
+  st = cuda_status(launch_pack(g, static_cast<uint8_t*>(packed), S(stream)));
+  if (st == TP_OK) *desc_out = d;
+  return st;
+}
+
+size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
+  (void)flags;
+  if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
+  return (size_t)(partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d));
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- forward paths
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+// Column-parallel half over token blocks of at most 64.
+tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
+                     int mode, cudaStream_t st) {
+  const int t = d->shape.t;
+  const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
+  const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
+  const size_t osz = mode == COLPAR_F32 ? 4 : 2;
+  for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
+    ColparArgs a{};
+    a.w = static_cast<const uint8_t*>(w);
+    a.shard_stride = d->shard_stride_bytes;
+    a.scales_offset = d->scales_offset;
+    a.rows = rows;
+    a.K = K;
+    a.t = t;
+    a.x = x + (size_t)m0 * K;
+    a.ldx = K;
+    a.M = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
+    a.out = static_cast<uint8_t*>(out) + (size_t)m0 * ldo * osz;
+    a.ldo = ldo;
+    a.mode = mode;
+    cudaError_t e = launch_colpar(a, d->wtype == TP_FP8_E4M3, st);
+    if (e != cudaSuccess) return TP_ERR_CUDA;
+  }
+  return TP_OK;
+}
+
+// Row-parallel half: partials_user != NULL -> write [t][M][N] partials only; otherwise fold
+// (in the CTA, by ticket, or unfused through tp_reduce_partials) into y with the residual.
+tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, int M,
+                     const bf16* res, bf16* y, float* partials_user, void* ws, size_t ws_bytes,
+                     uint32_t flags, cudaStream_t st) {
+  const int t = d->shape.t;
+  const int N = (int)d->rows_per_shard, K = (int)d->k_per_shard;
+  const RowparPlan plan = rowpar_plan(N, t);
+  if (plan.R == 0) return TP_ERR_ALIGN;
+  const bool unfused = (flags & TP_F_UNFUSED_REDUCE) != 0;
+  const bool need_ws = !partials_user && (unfused || plan.S > 1);
+  float* wsP = nullptr;
+  unsigned* tickets = nullptr;
+  if (need_ws) {
+    const uint64_t pb = partials_bytes(t, M, N);
+    if (!ws || ws_bytes < pb + ticket_bytes(N)) return TP_ERR_WORKSPACE;
+    if (!aligned16(ws)) return TP_ERR_ALIGN;
+    wsP = static_cast<float*>(ws);
+    tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pb);
+  }
+  for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
+    const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
+    RowparArgs a{};
+    a.w = static_cast<const uint8_t*>(w);
+    a.shard_stride = d->shard_stride_bytes;
+    a.scales_offset = d->scales_offset;
+    a.N = N;
+    a.K = K;
+    a.t = t;
+    a.x = a_in + (size_t)m0 * K * t;
+    a.ldx = K * t;
+    a.M = mb;
+    a.residual = res ? res + (size_t)m0 * N : nullptr;
+    a.y = y ? y + (size_t)m0 * N : nullptr;
+    a.ldy = N;
+    a.tickets = tickets;
+    if (partials_user) {
+      a.partials = partials_user + (size_t)m0 * N;
+      a.pM = M;
+      a.fold = FOLD_NONE;
+    } else if (unfused) {
+      a.partials = wsP;
+      a.pM = mb;
+      a.fold = FOLD_NONE;
+    } else {
+      a.partials = wsP;
+      a.pM = mb;
+      a.fold = plan.S == 1 ? FOLD_IN_CTA : FOLD_TICKET;
+    }
+    cudaError_t e = launch_rowpar(a, d->wtype == TP_FP8_E4M3, plan, st);
+    if (e != cudaSuccess) return TP_ERR_CUDA;
+    if (!partials_user && unfused) {
+      e = launch_reduce(wsP, t, mb, N, a.residual, a.y, st);
+      if (e != cudaSuccess) return TP_ERR_CUDA;
+    }
+  }
+  return TP_OK;
+}
+
+bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {
+  if (a.d != b.d || a.t != b.t || a.wtype != b.wtype) return false;
+  if (mlp) return a.ffn == b.ffn;
+  return a.n_q_heads == b.n_q_heads && a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim;
+}
+
+}  // namespace
+
+extern "C" {
+
+tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const void* x, int32_t M,
+                            void* out, uint32_t flags, void* stream) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  const int kind = desc->kind;
+  if (kind != TP_W_GATE_UP && kind != TP_W_QKV) return TP_ERR_INVALID_ARG;
+  tp_status st = check_desc(desc, kind, w);
+  if (st != TP_OK) return st;
+  if (M < 0 || (M > 0 && (!x || !out))) return TP_ERR_INVALID_ARG;
+  if (flags & ~(uint32_t)TP_F_FP32_COLPAR_OUT) return TP_ERR_INVALID_ARG;
+  const bool f32 = (flags & TP_F_FP32_COLPAR_OUT) != 0;
+  if (f32 && kind == TP_W_GATE_UP) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x) || !aligned16(out)) return TP_ERR_ALIGN;
+  const int mode = kind == TP_W_GATE_UP ? COLPAR_SWIGLU : (f32 ? COLPAR_F32 : COLPAR_BF16);
+  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream));
+}
+
+tp_status tp_rowpar_partials(const tp_packed_desc* desc, const void* w, const void* a, int32_t M,
+                             float* partials, void* stream) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  const int kind = desc->kind;
+  if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
+  tp_status st = check_desc(desc, kind, w);
+  if (st != TP_OK) return st;
+  if (M < 0 || (M > 0 && (!a || !partials))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(a) || !aligned16(partials)) return TP_ERR_ALIGN;
+  return run_rowpar(desc, w, static_cast<const bf16*>(a), M, nullptr, nullptr, partials, nullptr, 0,
+                    0, S(stream));
+}
+
+tp_status tp_rowpar_forward(const tp_packed_desc* desc, const void* w, const void* a,
+                            const void* residual, int32_t M, void* y, void* ws, size_t ws_bytes,
+                            uint32_t flags, void* stream) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  const int kind = desc->kind;
+  if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
+  tp_status st = check_desc(desc, kind, w);
+  if (st != TP_OK) return st;
+  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
+  return run_rowpar(desc, w, static_cast<const bf16*>(a), M, static_cast<const bf16*>(residual),
+                    static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, S(stream));
+}
+
+tp_status tp_reduce_partials(const float* partials, int32_t t, int32_t M, int32_t d,
+                             const void* residual, void* y, void* stream) {
+  if (t != 1 && t != 2 && t != 4 && t != 8) return TP_ERR_SHAPE;
+  if (M < 0 || d <= 0) return TP_ERR_INVALID_ARG;
+  if (M > 0 && (!partials || !y)) return TP_ERR_INVALID_ARG;
+  if (d % 8) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!aligned16(partials) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
+  return cuda_status(launch_reduce(partials, t, M, d, static_cast<const bf16*>(residual),
+                                   static_cast<bf16*>(y), S(stream)));
+}
+
+tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_packed_desc* dn,
+                         const void* dn_w, const void* x, const void* residual, int32_t M, void* y,
+                         void* h_out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  tp_status st = check_desc(gu, TP_W_GATE_UP, gu_w);
+  if (st != TP_OK) return st;
+  st = check_desc(dn, TP_W_DOWN, dn_w);
+  if (st != TP_OK) return st;
+  if (!same_block(gu->shape, dn->shape, true)) return TP_ERR_LAYOUT_MISMATCH;
+  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if (M < 0 || (M > 0 && (!x || !y || !h_out))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(h_out) || (residual && !aligned16(residual)))
+    return TP_ERR_ALIGN;
+  const RowparPlan plan = rowpar_plan(gu->shape.d, gu->shape.t);
+  if (((flags & TP_F_UNFUSED_REDUCE) || plan.S > 1) &&
+      (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)))
+    return TP_ERR_WORKSPACE;
+  cudaStream_t s = S(stream);
+  st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s);
+  if (st != TP_OK) return st;
+  return run_rowpar(dn, dn_w, static_cast<const bf16*>(h_out), M, static_cast<const bf16*>(residual),
+                    static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
+}
+
+tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp_packed_desc* o,
+                          const void* o_w, const void* x, const void* residual, int32_t M, void* y,
+                          void* qkv_out, void* o_in, void* ws, size_t ws_bytes, uint32_t flags,
+                          void* stream) {
+  tp_status st = check_desc(qkv, TP_W_QKV, qkv_w);
+  if (st != TP_OK) return st;
+  st = check_desc(o, TP_W_O, o_w);
+  if (st != TP_OK) return st;
+  if (!same_block(qkv->shape, o->shape, false)) return TP_ERR_LAYOUT_MISMATCH;
+  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if (M < 0 || (M > 0 && (!x || !y || !qkv_out || !o_in))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(qkv_out) || !aligned16(o_in) ||
+      (residual && !aligned16(residual)))
+    return TP_ERR_ALIGN;
+  const tp_shape& sh = qkv->shape;
+  const RowparPlan plan = rowpar_plan(sh.d, sh.t);
+  if (((flags & TP_F_UNFUSED_REDUCE) || plan.S > 1) &&
+      (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)))
+    return TP_ERR_WORKSPACE;
+  cudaStream_t s = S(stream);
+  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s);
+  if (st != TP_OK) return st;
+  st = cuda_status(launch_attn1(static_cast<const bf16*>(qkv_out), M, sh.n_q_heads, sh.n_kv_heads,
+                                sh.head_dim, sh.t, static_cast<bf16*>(o_in), s));
+  if (st != TP_OK) return st;
+  return run_rowpar(o, o_w, static_cast<const bf16*>(o_in), M, static_cast<const bf16*>(residual),
+                    static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
+}
+
+tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,
+                     void* stream) {
+  if (M < 0 || d <= 0 || !(eps >= 0.f)) return TP_ERR_INVALID_ARG;
+  if (M > 0 && (!x || !out)) return TP_ERR_INVALID_ARG;
+  if (d % 8) return TP_ERR_ALIGN;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x) || !aligned16(out) || (gain && !aligned16(gain))) return TP_ERR_ALIGN;
+  return cuda_status(launch_rmsnorm(static_cast<const bf16*>(x), static_cast<const bf16*>(gain), eps, M,
+                                    d, static_cast<bf16*>(out), S(stream)));
+}
+
+tp_status tp_sync(void* stream, int32_t timeout_ms) {
+  const auto deadline = std::chrono::steady_clock::now() + std::chrono::milliseconds(timeout_ms);
+  for (;;) {
+    const cudaError_t e = cudaStreamQuery(S(stream));
+    if (e == cudaSuccess) break;
+    if (e != cudaErrorNotReady) return TP_ERR_CUDA;
+    if (std::chrono::steady_clock::now() >= deadline) return TP_ERR_TIMEOUT;
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+  return TP_OK;
+}
+
+}  // extern "C"

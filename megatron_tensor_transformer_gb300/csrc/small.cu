@@ -1,0 +1,135 @@
+// The memory-bound pieces around the two GEMM halves: the shard fold ("all-reduce"),
+// RMSNorm, and the one-token attention stand-in that maps each shard's heads.
+#include "common.cuh"
+#include "small.h"
+
+#include <algorithm>
+
+namespace tpx {
+
+// y = bf16( ((P_0 + P_1) + ... + P_{t-1}) + residual ): Z = sum_k Z_k of the row-parallel
+// split ("Tensor Parallelism (Megatron-Style)", arunshar.com), folded in shard order so that
+// every run gives the same bits.  Four outputs per thread (d % 4 == 0).
+__global__ void reduce_kernel(const float* __restrict__ P, int t, size_t MN, int pstride_unused,
+                              const __nv_bfloat16* __restrict__ res, __nv_bfloat16* y) {
+  (void)pstride_unused;
+  const size_t n4 = MN / 4;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n4;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float4 v = __ldcs(reinterpret_cast<const float4*>(P) + i);
+    for (int s = 1; s < t; ++s) {
+      const float4 p = __ldcs(reinterpret_cast<const float4*>(P + (size_t)s * MN) + i);
+      v.x += p.x;
+      v.y += p.y;
+      v.z += p.z;
+      v.w += p.w;
+    }
+    if (res) {
+      const uint2 r = *reinterpret_cast<const uint2*>(res + 4 * i);
+      v.x += bf16_lo(r.x);
+      v.y += bf16_hi(r.x);
+      v.z += bf16_lo(r.y);
+      v.w += bf16_hi(r.y);
+    }
+    uint2 o;
+    o.x = (uint32_t)f2bf(v.x) | ((uint32_t)f2bf(v.y) << 16);
+    o.y = (uint32_t)f2bf(v.z) | ((uint32_t)f2bf(v.w) << 16);
+    *reinterpret_cast<uint2*>(y + 4 * i) = o;
+  }
+}
+
+cudaError_t launch_reduce(const float* P, int t, int M, int d, const __nv_bfloat16* res,
+                          __nv_bfloat16* y, cudaStream_t st) {
+  const size_t MN = (size_t)M * d;
+  const size_t n4 = MN / 4;
+  int blocks = (int)std::min<size_t>((n4 + 255) / 256, 152 * 8);
+  if (blocks < 1) blocks = 1;
+  reduce_kernel<<<blocks, 256, 0, st>>>(P, t, MN, 0, res, y);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// RMSNorm, one CTA per token: a = x / sqrt(mean(x^2) + eps) * g.  The sum of squares is
+// taken in a fixed order (per-thread strided sums, then a fixed tree) so runs repeat bitwise.
+__global__ void rmsnorm_kernel(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ gain,
+                               float eps, int d, __nv_bfloat16* out) {
+  __shared__ float part[32];
+  const int m = blockIdx.x;
+  const __nv_bfloat16* xr = x + (size_t)m * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      ss += a * a;
+      ss += b * b;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) part[0] = v;
+  }
+  __syncthreads();
+  const float inv = 1.0f / sqrtf(part[0] / (float)d + eps);
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 gv = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);  // 1.0 pairs
+    if (gain) gv = *reinterpret_cast<const uint4*>(gain + i);
+    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w[j]) * inv * bf16_lo(gw[j]);
+      const float b = bf16_hi(w[j]) * inv * bf16_hi(gw[j]);
+      o[j] = (uint32_t)f2bf(a) | ((uint32_t)f2bf(b) << 16);
+    }
+    *reinterpret_cast<uint4*>(out + (size_t)m * d + i) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, float eps, int M, int d,
+                           __nv_bfloat16* out, cudaStream_t st) {
+  rmsnorm_kernel<<<M, 256, 0, st>>>(x, gain, eps, d, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// One-token attention per shard: q head h (shard s = h / nq_s) returns the v of its kv group,
+// which lives in the same shard.  qkv is shard-major [q_s | k_s | v_s]; o_in is in head order.
+__global__ void attn1_kernel(const __nv_bfloat16* __restrict__ qkv, int M, int n_q, int n_kv, int hd,
+                             int t, __nv_bfloat16* o_in) {
+  const int nqs = n_q / t, nkvs = n_kv / t, group = n_q / n_kv;
+  const int Qs = (nqs + 2 * nkvs) * hd, Q = Qs * t;
+  const int vec_per_row = n_q * hd / 8;
+  const size_t total = (size_t)M * vec_per_row;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total;
+       i += (size_t)gridDim.x * blockDim.x) {
+    const int m = (int)(i / vec_per_row), v = (int)(i % vec_per_row);
+    const int col = v * 8, h = col / hd, e = col % hd;
+    const int s = h / nqs, hl = h % nqs, kvl = hl / group;
+    const size_t src = (size_t)m * Q + (size_t)s * Qs + (size_t)(nqs + nkvs) * hd + kvl * hd + e;
+    *reinterpret_cast<uint4*>(o_in + (size_t)m * n_q * hd + col) =
+        *reinterpret_cast<const uint4*>(qkv + src);
+  }
+}
+
+cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
+                         __nv_bfloat16* o_in, cudaStream_t st) {
+  const size_t total = (size_t)M * n_q * hd / 8;
+  int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 4);
+  if (blocks < 1) blocks = 1;
+  attn1_kernel<<<blocks, 256, 0, st>>>(qkv, M, n_q, n_kv, hd, t, o_in);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace tpx

@@ -1,0 +1,15 @@
+// Host-side interface of the fold / RMSNorm / attention stand-in kernels.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace tpx {
+
+cudaError_t launch_reduce(const float* P, int t, int M, int d, const __nv_bfloat16* res,
+                          __nv_bfloat16* y, cudaStream_t st);
+cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, float eps, int M, int d,
+                           __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
+                         __nv_bfloat16* o_in, cudaStream_t st);
+
+}  // namespace tpx

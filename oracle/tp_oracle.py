@@ -32,11 +32,12 @@ import numpy as np
 # --------------------------------------------------------------------------
 
 
-def bf16_bits_to_f64(bits):
-    """bf16 is the upper half of an IEEE binary32: 1 sign, 8 exponent, 7 mantissa bits."""
-    b = np.asarray(bits).astype(np.uint16)
-    sign = ((b >> 15) & 1).astype(np.float64)
-    e = ((b >> 7) & 0xFF).astype(np.int64)
+def _bf16_value(b):
+    """Value of one or more bf16 codes from the definition: the upper half of an IEEE binary32,
+    1 sign, 8 exponent (bias 127), 7 mantissa bits; exponent 0 is subnormal, 255 inf/NaN."""
+    b = np.asarray(b).astype(np.int64)
+    sign = (b >> 15) & 1
+    e = (b >> 7) & 0xFF
     m = (b & 0x7F).astype(np.float64)
     normal = np.ldexp(1.0 + m / 128.0, (e - 127).astype(np.int32))
     sub = np.ldexp(m / 128.0, -126)
@@ -44,6 +45,14 @@ def bf16_bits_to_f64(bits):
     v = np.where((e == 255) & (m == 0), np.inf, v)
     v = np.where((e == 255) & (m != 0), np.nan, v)
     return np.where(sign == 1, -v, v)
+
+
+_BF16_TABLE = _bf16_value(np.arange(65536))   # every code evaluated once from the definition
+
+
+def bf16_bits_to_f64(bits):
+    """bf16 codes (uint16) -> float64 values."""
+    return _BF16_TABLE[np.asarray(bits).astype(np.uint16)]
 
 
 def _round_to_grid(a, mant_bits, emin):
