@@ -285,7 +285,7 @@ def run_tpx(args, rank, world, local):
         "roofline": {"bound": "hbm", "kernel": "colpar_kernel (gate/up + SwiGLU)", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind + " (hbm_gbs, burst)", "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": None if tr is None else tr.get("bytes_per_launch_M64")},
+                     "traffic": None if tr is None else tr.get("bytes_per_launch")},
         "per_M": per_M,
         "cpu_baseline": cpu,
         "e2e": e2e,
