@@ -164,6 +164,27 @@ tp_status tp_rowpar_forward(const tp_packed_desc* desc /* host */, const void* w
                             const void* residual, int32_t M, void* y, void* ws, size_t ws_bytes,
                             uint32_t flags, void* stream);
 
+/* Allocation-free variant of tp_rowpar_forward.  The pages have no counterpart: this
+ * entry point exists for callers that cannot allocate device memory, such as a plugin
+ * inside a host framework whose caching allocator owns the whole device, or code on a
+ * latency-critical path that cannot afford cudaMalloc's implicit synchronisation.
+ * Same arguments, result and bits as tp_rowpar_forward, minus the workspace: the shard
+ * partials and tickets live in one static device array of tp_noalloc_scratch_capacity()
+ * bytes (16 MiB), which every GPU that loads the library holds until the process exits.
+ * Requests that need more (t * min(M,64) * N * 4 bytes plus N/2 bytes of tickets)
+ * return TP_ERR_WORKSPACE.  The call never allocates or frees memory.  The first call on
+ * each device resolves the array's device address (cudaGetSymbolAddress, with that
+ * device current), so make that first call before any stream capture.  Every call on a
+ * device shares the one array and leaves its contents behind (the tickets are cleared
+ * at the start of each call): calls that may overlap on the GPU (other streams, other
+ * threads) race and must be serialised by the caller. */
+tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc /* host */, const void* w, const void* a,
+                                    const void* residual, int32_t M, void* y, uint32_t flags,
+                                    void* stream);
+
+/* Bytes of the static scratch array tp_rowpar_forward_noalloc uses. */
+size_t tp_noalloc_scratch_capacity(void);
+
 /* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g). */
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,
                      void* stream);

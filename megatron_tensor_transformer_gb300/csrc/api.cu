@@ -1,6 +1,7 @@
 // C ABI of libtpx.so: argument checks, packed-weight descriptors, kernel dispatch.
 // Every check runs on the host before anything is enqueued.
 #include <atomic>
+#include <mutex>
 #include <chrono>
 #include <cstring>
 #include <thread>
@@ -422,3 +423,64 @@ tp_status tp_sync(void* stream, int32_t timeout_ms) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free row-parallel
+//
+// Some callers cannot allocate device memory: a plugin living inside a host framework
+// whose caching allocator owns the whole device (a side cudaMalloc fragments its pool
+// or is forbidden), or code on a latency-critical path where cudaMalloc's implicit
+// synchronisation is not acceptable.  tp_rowpar_forward_noalloc serves them: its scratch
+// (shard partials and row-tile tickets) lives in the file-scope array below, so the call
+// allocates nothing.  Every GPU that loads the library holds this array until exit.
+
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 16u << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char tpx_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[128] = {};  // device address of the array, per device ordinal
+
+// Host code cannot use the array's name as a device address: resolve it once per device,
+// with that device current.
+tp_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return TP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, tpx_noalloc_scratch) != cudaSuccess || !p) return TP_ERR_CUDA;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TP_OK;
+}
+
+}  // namespace
+
+extern "C" size_t tp_noalloc_scratch_capacity(void) { return kNoallocScratchBytes; }
+
+extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const void* w, const void* a,
+                                               const void* residual, int32_t M, void* y, uint32_t flags,
+                                               void* stream) {
+  if (!desc) return TP_ERR_INVALID_ARG;
+  const int kind = desc->kind;
+  if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
+  tp_status st = check_desc(desc, kind, w);
+  if (st != TP_OK) return st;
+  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
+  const int t = desc->shape.t, N = (int)desc->rows_per_shard;
+  const uint64_t pb = partials_bytes(t, M, N), need = pb + ticket_bytes(N);
+  if (need > kNoallocScratchBytes) return TP_ERR_WORKSPACE;  // beyond the static scratch
+  void* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != TP_OK) return st;
+  // the tickets must start at zero; the partials are fully written before they are read
+  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + pb, 0, ticket_bytes(N), S(stream)) != cudaSuccess)
+    return TP_ERR_CUDA;
+  return run_rowpar(desc, w, static_cast<const bf16*>(a), M, static_cast<const bf16*>(residual),
+                    static_cast<bf16*>(y), nullptr, scratch, (size_t)need, flags, S(stream));
+}

@@ -20,7 +20,8 @@ TP_F_UNFUSED_REDUCE, TP_F_FP32_COLPAR_OUT = 0x1, 0x2
 
 EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspace_bytes",
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
-           "tp_rowpar_partials", "tp_rowpar_forward", "tp_rmsnorm", "tp_sync", "tp_status_str", "tp_launch_count"]
+           "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
+           "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_sync", "tp_status_str", "tp_launch_count"]
 
 
 class TpxError(RuntimeError):
@@ -65,6 +66,8 @@ def lib():
             "tp_colpar_forward": (I32, [P(PackedDesc), V, V, I32, V, U32, V]),
             "tp_rowpar_partials": (I32, [P(PackedDesc), V, V, I32, V, V]),
             "tp_rowpar_forward": (I32, [P(PackedDesc), V, V, V, I32, V, V, SZ, U32, V]),
+            "tp_rowpar_forward_noalloc": (I32, [P(PackedDesc), V, V, V, I32, V, U32, V]),
+            "tp_noalloc_scratch_capacity": (SZ, []),
             "tp_rmsnorm": (I32, [V, V, ctypes.c_float, I32, I32, V, V]),
             "tp_sync": (I32, [V, I32]),
             "tp_status_str": (ctypes.c_char_p, [I32]),
@@ -176,6 +179,18 @@ def tp_rowpar_forward(desc, w, a, residual, y, ws, flags=0, stream=None):
                                    _ptr(ws), 0 if ws is None else ws.numel(), flags, _stream(stream)),
            "tp_rowpar_forward")
     return y
+
+
+def tp_rowpar_forward_noalloc(desc, w, a, residual, y, flags=0, stream=None):
+    """tp_rowpar_forward without a workspace argument: for callers that cannot allocate
+    device memory (the library's own static scratch array is used)."""
+    _check(lib().tp_rowpar_forward_noalloc(ctypes.byref(desc), _ptr(w), _ptr(a), _ptr(residual), a.shape[0],
+                                           _ptr(y), flags, _stream(stream)), "tp_rowpar_forward_noalloc")
+    return y
+
+
+def tp_noalloc_scratch_capacity():
+    return lib().tp_noalloc_scratch_capacity()
 
 
 def tp_rmsnorm(x, out, eps=1e-5, gain=None, stream=None):
