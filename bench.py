@@ -222,6 +222,7 @@ def run_tpx(args, rank, world, local):
     hs = {M: torch.empty((M, FFN), dtype=torch.bfloat16, device=dev) for M in MS}
     ys = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
     ws = tpx.new_workspace(sh, max(MS), dev)
+    kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY}[args.kernel]
     K = args.steps
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in MS] for _ in range(K)]
 
@@ -229,10 +230,10 @@ def run_tpx(args, rank, world, local):
         for j, M in enumerate(MS):
             if i is not None:
                 ev[i][j][0].record(stream)
-            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], stream=stream)
+            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], flags=kf, stream=stream)
             if i is not None:
                 ev[i][j][1].record(stream)
-            tpx.tp_rowpar_forward(dn, dn_w, hs[M], xs[M], ys[M], ws, stream=stream)
+            tpx.tp_rowpar_forward(dn, dn_w, hs[M], xs[M], ys[M], ws, flags=kf, stream=stream)
             if i is not None:
                 ev[i][j][2].record(stream)
 
@@ -339,6 +340,8 @@ def main():
     ap.add_argument("--impl", default="tpx", choices=["tpx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny"],
+                    help="force the tcgen05 or the mma.sync decode kernel (default: library policy)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

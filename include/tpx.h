@@ -96,6 +96,9 @@ typedef struct {
 #define TP_F_UNFUSED_REDUCE 0x1u  /* row-parallel: write shard partials to the workspace, then
                                      run tp_reduce_partials (same bits as the fused path) */
 #define TP_F_FP32_COLPAR_OUT 0x2u /* tp_colpar_forward: write fp32 instead of bf16 */
+#define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
+#define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernel (bf16 weights, rows % 128, K % 64);
+                                     default: tcgen05 where supported for M > 16, else mma.sync */
 
 /* Size in bytes of the packed buffer for (shape, kind); 0 if the shape is invalid. */
 size_t tp_packed_bytes(const tp_shape* shape /* host */, int32_t kind);

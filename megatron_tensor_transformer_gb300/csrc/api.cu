@@ -10,6 +10,7 @@
 #include "pack.h"
 #include "skinny.h"
 #include "small.h"
+#include "tc.h"
 
 namespace tpx {
 static std::atomic<uint64_t> g_launches{0};
@@ -190,13 +191,42 @@ namespace {
 
 using bf16 = __nv_bfloat16;
 
-// Column-parallel half over token blocks of at most 64.
+// Kernel choice: the tcgen05 GEMM where the geometry allows it and M is above the
+// threshold, the mma.sync skinny kernel otherwise; flags can force either one.
+constexpr int kTcMinM = 16;
+constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
+
+bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
+  if (flags & TP_F_KERNEL_SKINNY) return false;
+  if (!tc_supported(rows, K, fp8)) return false;
+  if (flags & TP_F_KERNEL_TC) return true;
+  return M > kTcMinM;
+}
+
+bool bad_kernel_flags(uint32_t flags) { return (flags & kKernelFlags) == kKernelFlags; }
+
+// Column-parallel half over token blocks of at most 64 (skinny) or all tokens (tcgen05).
 tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
-                     int mode, cudaStream_t st) {
+                     int mode, cudaStream_t st, uint32_t flags = 0) {
   const int t = d->shape.t;
   const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
   const size_t osz = mode == COLPAR_F32 ? 4 : 2;
+  if (pick_tc(flags, rows, K, d->wtype == TP_FP8_E4M3, M)) {
+    TcArgs a{};
+    a.mode = mode == COLPAR_SWIGLU ? TC_COLPAR_SWIGLU : (mode == COLPAR_F32 ? TC_COLPAR_F32 : TC_COLPAR_BF16);
+    a.w = static_cast<const uint8_t*>(w);
+    a.shard_stride = d->shard_stride_bytes;
+    a.t = t;
+    a.rows = rows;
+    a.K = K;
+    a.x = x;
+    a.ldx = K;
+    a.M = M;
+    a.out = out;
+    a.ldo = ldo;
+    return launch_tc(a, st) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
     ColparArgs a{};
     a.w = static_cast<const uint8_t*>(w);
@@ -227,7 +257,8 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   const RowparPlan plan = rowpar_plan(N, t);
   if (plan.R == 0) return TP_ERR_ALIGN;
   const bool unfused = (flags & TP_F_UNFUSED_REDUCE) != 0;
-  const bool need_ws = !partials_user && (unfused || plan.S > 1);
+  const bool tc = pick_tc(flags, N, K, d->wtype == TP_FP8_E4M3, M);
+  const bool need_ws = !partials_user && (unfused || plan.S > 1 || tc);
   float* wsP = nullptr;
   unsigned* tickets = nullptr;
   if (need_ws) {
@@ -236,6 +267,43 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     if (!aligned16(ws)) return TP_ERR_ALIGN;
     wsP = static_cast<float*>(ws);
     tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pb);
+  }
+  if (tc) {
+    TcArgs a{};
+    a.w = static_cast<const uint8_t*>(w);
+    a.shard_stride = d->shard_stride_bytes;
+    a.t = t;
+    a.rows = N;
+    a.K = K;
+    a.ldx = K * t;
+    a.ldy = N;
+    a.tickets = tickets;
+    if (partials_user || (!unfused && M > kSkinnyMaxM)) {
+      // one launch over all tokens: partials only, or every shard chained in one accumulator
+      a.mode = partials_user ? TC_ROWPAR_SHARD : TC_ROWPAR_CHAIN;
+      a.x = a_in;
+      a.M = M;
+      a.residual = res;
+      a.y = y;
+      a.partials = partials_user;
+      a.pM = M;
+      a.fold = 0;
+      return launch_tc(a, st) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    }
+    for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {  // per-shard partials in the workspace
+      const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
+      a.mode = TC_ROWPAR_SHARD;
+      a.x = a_in + (size_t)m0 * K * t;
+      a.M = mb;
+      a.residual = res ? res + (size_t)m0 * N : nullptr;
+      a.y = y + (size_t)m0 * N;
+      a.partials = wsP;
+      a.pM = mb;
+      a.fold = unfused ? 0 : 1;
+      if (launch_tc(a, st) != cudaSuccess) return TP_ERR_CUDA;
+      if (unfused && launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
+    }
+    return TP_OK;
   }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
     const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
@@ -294,13 +362,14 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
   if (M < 0 || (M > 0 && (!x || !out))) return TP_ERR_INVALID_ARG;
-  if (flags & ~(uint32_t)TP_F_FP32_COLPAR_OUT) return TP_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(TP_F_FP32_COLPAR_OUT | kKernelFlags)) || bad_kernel_flags(flags))
+    return TP_ERR_INVALID_ARG;
   const bool f32 = (flags & TP_F_FP32_COLPAR_OUT) != 0;
   if (f32 && kind == TP_W_GATE_UP) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(x) || !aligned16(out)) return TP_ERR_ALIGN;
   const int mode = kind == TP_W_GATE_UP ? COLPAR_SWIGLU : (f32 ? COLPAR_F32 : COLPAR_BF16);
-  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream));
+  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags);
 }
 
 tp_status tp_rowpar_partials(const tp_packed_desc* desc, const void* w, const void* a, int32_t M,
@@ -325,7 +394,8 @@ tp_status tp_rowpar_forward(const tp_packed_desc* desc, const void* w, const voi
   if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
-  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+    return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
@@ -353,17 +423,15 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
   st = check_desc(dn, TP_W_DOWN, dn_w);
   if (st != TP_OK) return st;
   if (!same_block(gu->shape, dn->shape, true)) return TP_ERR_LAYOUT_MISMATCH;
-  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+    return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!x || !y || !h_out))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(x) || !aligned16(y) || !aligned16(h_out) || (residual && !aligned16(residual)))
     return TP_ERR_ALIGN;
-  const RowparPlan plan = rowpar_plan(gu->shape.d, gu->shape.t);
-  if (((flags & TP_F_UNFUSED_REDUCE) || plan.S > 1) &&
-      (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)))
-    return TP_ERR_WORKSPACE;
+  if (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
-  st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s);
+  st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags);
   if (st != TP_OK) return st;
   return run_rowpar(dn, dn_w, static_cast<const bf16*>(h_out), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
@@ -378,19 +446,17 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
   st = check_desc(o, TP_W_O, o_w);
   if (st != TP_OK) return st;
   if (!same_block(qkv->shape, o->shape, false)) return TP_ERR_LAYOUT_MISMATCH;
-  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+    return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!x || !y || !qkv_out || !o_in))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(x) || !aligned16(y) || !aligned16(qkv_out) || !aligned16(o_in) ||
       (residual && !aligned16(residual)))
     return TP_ERR_ALIGN;
   const tp_shape& sh = qkv->shape;
-  const RowparPlan plan = rowpar_plan(sh.d, sh.t);
-  if (((flags & TP_F_UNFUSED_REDUCE) || plan.S > 1) &&
-      (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)))
-    return TP_ERR_WORKSPACE;
+  if (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
-  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s);
+  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags);
   if (st != TP_OK) return st;
   st = cuda_status(launch_attn1(static_cast<const bf16*>(qkv_out), M, sh.n_q_heads, sh.n_kv_heads,
                                 sh.head_dim, sh.t, static_cast<bf16*>(o_in), s));
@@ -419,6 +485,7 @@ tp_status tp_sync(void* stream, int32_t timeout_ms) {
     if (std::chrono::steady_clock::now() >= deadline) return TP_ERR_TIMEOUT;
     std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
+  if (tc_take_device_error() != 0) return TP_ERR_DEVICE_TIMEOUT;
   return TP_OK;
 }
 
@@ -468,7 +535,8 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
-  if (flags & ~(uint32_t)TP_F_UNFUSED_REDUCE) return TP_ERR_INVALID_ARG;
+  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+    return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;

@@ -1,0 +1,420 @@
+// tcgen05 weight-streaming GEMM for the column- and row-parallel linears.
+//
+// D[weight rows, tokens] = W_s[rows, K] * X[tokens, K]^T for one shard s: the weights are
+// the MMA's A operand (128 rows per tile, K-major) and the tokens its B operand (BN per
+// tile, K-major), so one kernel serves decode (BN = 16..64 tokens, weight-streaming, HBM
+// bound) and prefill (BN = 256 token tiles, tensor bound).  The column split of the first
+// linear and the row split of the second ("ColumnParallelLinear" / "RowParallelLinear",
+// scalablesystem.dev, "The Tensor-Parallel Shard Group") only change which shard buffer
+// and which activation columns a tile reads, and what the epilogue does:
+//   colpar:      store D (or silu(g) * u for interleaved gate/up rows) for shard s;
+//   rowpar:      per-(tile, shard) partial P_s, then the last shard to finish folds
+//                ((P_0 + P_1) + ...) + residual in shard order (Z = sum_k Z_k);
+//   rowpar-chain (large M): all shards' k-blocks accumulate into one TMEM tile in shard
+//                order, + residual (no partials round trip through memory).
+//
+// Structure: persistent CTAs (one per SM), warp roles:
+//   warps 0-3  epilogue: TMEM -> registers -> global (lane i of warp w = tile row 32w+i)
+//   warp 4     producer: one thread issues TMA tensor copies into a ring of smem stages
+//   warp 5     MMA: one thread issues tcgen05.mma (4 per 64-wide k-block) into a
+//              double-buffered TMEM accumulator; tcgen05.commit frees stages / hands off
+// Every wait is an mbarrier poll bounded in time; on expiry the kernel records an error
+// word, drains what it issued, frees its TMEM and returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "tc.h"
+#include "tc_ptx.cuh"
+
+namespace tpx {
+using namespace tc;
+
+static __device__ unsigned g_tc_error;
+
+constexpr int BM = 128, BK = 64;
+constexpr int kThreads = 192, kProducerWarp = 4, kMmaWarp = 5;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr int kBarBytes = 256;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+};
+
+struct Geo {  // item geometry shared by the three roles
+  int n_rt, n_tt, n_items, kb_per_shard, nkb;
+};
+
+__device__ __forceinline__ Geo make_geo(const TcArgs& a, int BN) {
+  Geo g;
+  g.n_rt = a.rows / BM;
+  g.n_tt = (a.M + BN - 1) / BN;
+  g.kb_per_shard = a.K / BK;
+  if (a.mode == TC_ROWPAR_CHAIN) {
+    g.n_items = g.n_rt * g.n_tt;
+    g.nkb = g.kb_per_shard * a.t;
+  } else {
+    g.n_items = g.n_rt * g.n_tt * a.t;
+    g.nkb = g.kb_per_shard;
+  }
+  return g;
+}
+
+// item -> (shard, row tile, token tile).  Column-parallel items walk token tiles fastest (a
+// weight tile is reused from L2 by concurrent CTAs); row-parallel items walk shards fastest
+// (the t partials of a tile finish close together).
+__device__ __forceinline__ void decode_item(const TcArgs& a, const Geo& g, int i, int& s, int& rt, int& tt) {
+  if (a.mode == TC_ROWPAR_CHAIN) {
+    s = 0;
+    tt = i % g.n_tt;
+    rt = i / g.n_tt;
+  } else if (a.mode == TC_ROWPAR_SHARD) {
+    s = i % a.t;
+    tt = (i / a.t) % g.n_tt;
+    rt = i / (a.t * g.n_tt);
+  } else {
+    tt = i % g.n_tt;
+    rt = (i / g.n_tt) % g.n_rt;
+    s = i / (g.n_tt * g.n_rt);
+  }
+}
+
+__device__ __forceinline__ void raise_error(unsigned code, volatile int* abort_flag) {
+  atomicExch(&g_tc_error, code);
+  *abort_flag = 1;
+}
+
+// One 16-column chunk of the accumulator for tile row p (of shard s), tokens mf..mf+15.
+template <int BN>
+__device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, int mf, const float (&v)[16]) {
+  if (a.mode == TC_COLPAR_SWIGLU) {
+    // rows come as [8 gate | 8 up] blocks: the up value of row p sits 8 lanes further on
+    float u[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = __shfl_down_sync(0xffffffffu, v[j], 8);
+    if ((p & 15) < 8) {
+      const int f = s * (a.rows / 2) + (p >> 4) * 8 + (p & 7);
+      uint16_t* o = reinterpret_cast<uint16_t*>(a.out);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (mf + j < a.M) o[(size_t)(mf + j) * a.ldo + f] = f2bf(silu_f(v[j]) * u[j]);
+    }
+  } else if (a.mode == TC_COLPAR_BF16 || a.mode == TC_COLPAR_F32) {
+    const size_t col = (size_t)s * a.rows + p;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (mf + j >= a.M) break;
+      const size_t o = (size_t)(mf + j) * a.ldo + col;
+      if (a.mode == TC_COLPAR_F32)
+        reinterpret_cast<float*>(a.out)[o] = v[j];
+      else
+        reinterpret_cast<uint16_t*>(a.out)[o] = f2bf(v[j]);
+    }
+  } else if (a.mode == TC_ROWPAR_SHARD) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (mf + j < a.M) a.partials[((size_t)s * a.pM + mf + j) * a.rows + p] = v[j];
+  } else {  // TC_ROWPAR_CHAIN: the whole fold is in v already
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (mf + j >= a.M) break;
+      const size_t o = (size_t)(mf + j) * a.ldy + p;
+      float val = v[j];
+      if (a.residual) val += __bfloat162float(a.residual[o]);
+      reinterpret_cast<uint16_t*>(a.y)[o] = f2bf(val);
+    }
+  }
+}
+
+// After the t shard partials of (row tile rt, token tile tt) are stored, the last CTA to
+// finish one of them folds ((P_0 + P_1) + ...) + residual into y.  No CTA waits for another.
+template <int BN>
+__device__ bool rowpar_fold(const TcArgs& a, const Geo& g, int rt, int tt, int p, uint32_t epi_bar,
+                            int& phase, volatile int* last_flag, volatile int* abort_flag) {
+  __threadfence();
+  mbar_arrive(epi_bar);
+  if (!mbar_wait(epi_bar, phase)) {
+    raise_error(7, abort_flag);
+    return false;
+  }
+  phase ^= 1;
+  const int slot = rt * g.n_tt + tt;
+  if (threadIdx.x == 0) {
+    const unsigned old = atomicAdd(&a.tickets[slot], 1u);
+    *last_flag = old == (unsigned)(a.t - 1);
+  }
+  mbar_arrive(epi_bar);
+  if (!mbar_wait(epi_bar, phase)) {
+    raise_error(8, abort_flag);
+    return false;
+  }
+  phase ^= 1;
+  if (*last_flag) {
+    __threadfence();
+    const int m1 = min(a.M, (tt + 1) * BN);
+    for (int m = tt * BN; m < m1; ++m) {
+      const size_t pn = (size_t)m * a.rows + p;
+      float v = __ldcg(a.partials + pn);
+      for (int s = 1; s < a.t; ++s) v += __ldcg(a.partials + (size_t)s * a.pM * a.rows + pn);
+      const size_t o = (size_t)m * a.ldy + p;
+      if (a.residual) v += __bfloat162float(a.residual[o]);
+      reinterpret_cast<uint16_t*>(a.y)[o] = f2bf(v);
+    }
+    if (threadIdx.x == 0) a.tickets[slot] = 0u;
+  }
+  return true;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+  using C = TcCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                                   // S x [128 rows x 64] bf16, SW128
+  uint8_t* sB = smem + (size_t)S * C::kABytes;          // S x [BN rows x 64] bf16, SW128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], epi, drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 3);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
+                 tempty0 = smem_u32(bars + 2 * S + 2), epi_bar = smem_u32(bars + 2 * S + 4),
+                 drain_bar = smem_u32(bars + 2 * S + 5);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Geo g = make_geo(a, BN);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);  // one arrival per epilogue warp
+    }
+    mbar_init(epi_bar, 128);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    *mma_consumed = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducerWarp && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  int issued = 0;  // producer: k-blocks issued
+
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+        int s, rt, tt;
+        decode_item(a, g, item, s, rt, tt);
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          const int st = issued % S;
+          if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+            raise_error(1, abort_flag);
+            break;
+          }
+          const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
+          const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
+          const int xcol = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kStageBytes);
+          tma_load_3d(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st);
+          tma_load_2d(smem_u32(sB + (size_t)st * C::kBBytes), &tmB, xcol, tt * BN, full0 + 8 * st);
+          ++issued;
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      int consumed = 0, it = 0;
+      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x, ++it) {
+        const int acc = it & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) {
+          raise_error(2, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          const int st = consumed % S;
+          if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1)) {
+            raise_error(3, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)st * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb | k) != 0);
+          mma_commit(empty0 + 8 * st);  // the stage is free once these MMAs have read it
+          ++consumed;
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);   // accumulator ready for the epilogue
+      }
+      *mma_consumed = consumed;
+      // wait for every MMA this thread issued before the TMEM can be released
+      mma_commit(drain_bar);
+      if (!mbar_wait(drain_bar, 0)) raise_error(4, abort_flag);
+    }
+  } else {
+    // epilogue warps 0..3
+    const int r = warp * 32 + lane;  // row inside the 128-row tile
+    int it = 0, epi_phase = 0;
+    for (int item = blockIdx.x; item < g.n_items; item += gridDim.x, ++it) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      int s, rt, tt;
+      decode_item(a, g, item, s, rt, tt);
+      const int acc = it & 1;
+      // warp-uniform: the tcgen05.ld below is a warp-collective instruction
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
+        raise_error(5, abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
+      const int p = rt * BM + r;  // row of the shard's matrix
+      const int m0 = tt * BN;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tb + c0, v);
+        tmem_ld_wait();
+        epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (a.mode == TC_ROWPAR_SHARD && a.fold) {
+        if (!rowpar_fold<BN>(a, g, rt, tt, p, epi_bar, epi_phase, last_flag, abort_flag)) break;
+      }
+    }
+  }
+
+  __syncthreads();
+  // drain: wait (bounded) for any TMA copy issued but never consumed, so that no copy
+  // lands in shared memory after the CTA has exited
+  if (warp == kProducerWarp && lane == 0) {
+    for (int q = *mma_consumed; q < issued; ++q)
+      if (!mbar_wait(full0 + 8 * (q % S), (q / S) & 1)) {
+        atomicExch(&g_tc_error, 6u);
+        break;
+      }
+  }
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiled encode_fn() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+bool tc_supported(int rows, int K, bool fp8) { return !fp8 && rows % BM == 0 && K % BK == 0 && K > 0; }
+
+int tc_ticket_slots(int rows, int M) { return rows / BM * ((M + 15) / 16); }
+
+unsigned tc_take_device_error() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_tc_error, &z, sizeof(z));
+  return v;
+}
+
+template <int BN>
+static cudaError_t tc_go(const TcArgs& a, cudaStream_t st) {
+  using C = TcCfg<BN>;
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tmA, tmB;
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.rows, (cuuint64_t)a.t};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, (cuuint64_t)a.shard_stride};
+    const cuuint32_t box[3] = {BK, BM, 1}, es[3] = {1, 1, 1};
+    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.ldx, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.ldx * 2};
+    const cuuint32_t box[2] = {BK, BN}, es[2] = {1, 1};
+    if (enc(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;  // per instantiation; set before the first launch
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int n_rt = a.rows / BM, n_tt = (a.M + BN - 1) / BN;
+  const int n_items = a.mode == TC_ROWPAR_CHAIN ? n_rt * n_tt : n_rt * n_tt * a.t;
+  const int grid = n_items < sm_count() ? n_items : sm_count();
+  tc_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(tmA, tmB, a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t st) {
+  if (!tc_supported(a.rows, a.K, false) || a.M <= 0) return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x)) & 15) return cudaErrorInvalidValue;
+  if (a.M <= 16) return tc_go<16>(a, st);
+  if (a.M <= 32) return tc_go<32>(a, st);
+  if (a.M <= 64) return tc_go<64>(a, st);
+  if (a.M <= 128) return tc_go<128>(a, st);
+  return tc_go<256>(a, st);
+}
+
+}  // namespace tpx

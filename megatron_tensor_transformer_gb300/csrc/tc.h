@@ -1,0 +1,44 @@
+// Host-side interface of the tcgen05 weight-streaming GEMM (weights on the MMA's M side).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tpx {
+
+enum TcMode {
+  TC_COLPAR_BF16 = 0,    // out[m][s*rows + r] = bf16(D)
+  TC_COLPAR_F32 = 1,     // same, fp32
+  TC_COLPAR_SWIGLU = 2,  // gate/up rows interleaved by 8: out[m][s*rows/2 + f] = bf16(silu(g) u)
+  TC_ROWPAR_SHARD = 3,   // per-(tile, shard) item: partial P_s, then the last shard folds (or not)
+  TC_ROWPAR_CHAIN = 4    // per-tile item: all shards' k chained in one accumulator, + residual
+};
+
+struct TcArgs {
+  int mode;
+  const uint8_t* w;          // packed weights, shard 0
+  uint64_t shard_stride;     // bytes
+  int t, rows, K;            // shards; per-shard matrix [rows, K]
+  const __nv_bfloat16* x;    // activations [M, ldx]
+  int ldx, M;
+  void* out;                 // colpar output
+  int ldo;
+  // row-parallel
+  const __nv_bfloat16* residual;  // nullable, [M, ldy]
+  __nv_bfloat16* y;               // [M, ldy]
+  int ldy;
+  float* partials;                // [t][pM][rows]
+  int pM;
+  unsigned* tickets;              // one per (row tile, token tile), zero between launches
+  int fold;                       // TC_ROWPAR_SHARD: 1 = last shard folds into y, 0 = partials only
+};
+
+// Whether the tcgen05 path supports this geometry (rows % 128, K % 64, bf16 weights).
+bool tc_supported(int rows, int K, bool fp8);
+// Ticket slots TC_ROWPAR_SHARD needs for (rows, M).
+int tc_ticket_slots(int rows, int M);
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t st);
+// Device error word set by a bounded wait that gave up (0 = none); read and cleared.
+unsigned tc_take_device_error();
+
+}  // namespace tpx
