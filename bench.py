@@ -230,7 +230,7 @@ def run_tpx(args, rank, world, local):
         for j, M in enumerate(MS):
             if i is not None:
                 ev[i][j][0].record(stream)
-            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], flags=kf, stream=stream)
+            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], flags=kf, stream=stream, ws=ws)
             if i is not None:
                 ev[i][j][1].record(stream)
             tpx.tp_rowpar_forward(dn, dn_w, hs[M], xs[M], ys[M], ws, flags=kf, stream=stream)

@@ -150,9 +150,10 @@ tp_status tp_reduce_partials(const float* partials, int32_t t, int32_t M, int32_
 
 /* Column-parallel building block: out[m][s*rows + r] for every shard s and packed row r.
  * GATE_UP: out = h [M, ffn] bf16 (SwiGLU applied);  QKV: out = qkv [M, Q] bf16.
- * With TP_F_FP32_COLPAR_OUT (QKV only) out is fp32. */
+ * With TP_F_FP32_COLPAR_OUT (QKV only) out is fp32.  ws is optional (NULL, or a workspace of
+ * tp_workspace_bytes(shape, M) bytes, which lets the tcgen05 kernel balance work across SMs). */
 tp_status tp_colpar_forward(const tp_packed_desc* desc /* host */, const void* w, const void* x,
-                            int32_t M, void* out, uint32_t flags, void* stream);
+                            int32_t M, void* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
 /* Row-parallel building block without the fold: partials[s][m][n] = (a_s W_s)[m][n],
  * a_s = columns [s*K_s, (s+1)*K_s) of a [M, t*K_s] bf16; partials [t][M][N] fp32. */
@@ -173,9 +174,9 @@ tp_status tp_rowpar_forward(const tp_packed_desc* desc /* host */, const void* w
  * latency-critical path that cannot afford cudaMalloc's implicit synchronisation.
  * Same arguments, result and bits as tp_rowpar_forward, minus the workspace: the shard
  * partials and tickets live in one static device array of tp_noalloc_scratch_capacity()
- * bytes (16 MiB), which every GPU that loads the library holds until the process exits.
- * Requests that need more (t * min(M,64) * N * 4 bytes plus N/2 bytes of tickets)
- * return TP_ERR_WORKSPACE.  The call never allocates or frees memory.  The first call on
+ * bytes (32 MiB), which every GPU that loads the library holds until the process exits.
+ * Requests that need more (t * min(M,64) * N * 4 bytes of partials, N/2 bytes of tickets
+ * and 10.5 MB of work-balancing scratch) return TP_ERR_WORKSPACE.  The call never allocates or frees memory.  The first call on
  * each device resolves the array's device address (cudaGetSymbolAddress, with that
  * device current), so make that first call before any stream capture.  Every call on a
  * device shares the one array and leaves its contents behind (the tickets are cleared

@@ -180,7 +180,7 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
 size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
   (void)flags;
   if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
-  return (size_t)(partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d));
+  return (size_t)(partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d) + align_up(tc_streamk_bytes()));
 }
 
 }  // extern "C"
@@ -194,6 +194,7 @@ using bf16 = __nv_bfloat16;
 // Kernel choice: the tcgen05 GEMM where the geometry allows it and M is above the
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 16;
+constexpr int kTcFoldMaxM = 16;  // tcgen05 row-parallel: fold in the kernel up to this many tokens
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
@@ -205,9 +206,17 @@ bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
 
 bool bad_kernel_flags(uint32_t flags) { return (flags & kKernelFlags) == kKernelFlags; }
 
+// Stream-K scratch of the tcgen05 kernel: [pieces][item tickets], or none.
+void set_streamk(TcArgs& a, void* sk_ws) {
+  if (!sk_ws) return;
+  a.pieces = static_cast<float*>(sk_ws);
+  a.item_tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(sk_ws) + tc_streamk_bytes() -
+                                               (size_t)kTcMaxStreamkItems * 4);
+}
+
 // Column-parallel half over token blocks of at most 64 (skinny) or all tokens (tcgen05).
 tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
-                     int mode, cudaStream_t st, uint32_t flags = 0) {
+                     int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr) {
   const int t = d->shape.t;
   const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
@@ -225,6 +234,7 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     a.M = M;
     a.out = out;
     a.ldo = ldo;
+    set_streamk(a, sk_ws);
     return launch_tc(a, st) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
   }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
@@ -268,6 +278,9 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     wsP = static_cast<float*>(ws);
     tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pb);
   }
+  void* sk_ws = nullptr;
+  if (need_ws && ws_bytes >= partials_bytes(t, M, N) + ticket_bytes(N) + tc_streamk_bytes())
+    sk_ws = static_cast<uint8_t*>(ws) + partials_bytes(t, M, N) + ticket_bytes(N);
   if (tc) {
     TcArgs a{};
     a.w = static_cast<const uint8_t*>(w);
@@ -278,6 +291,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     a.ldx = K * t;
     a.ldy = N;
     a.tickets = tickets;
+    set_streamk(a, sk_ws);
     if (partials_user || (!unfused && M > kSkinnyMaxM)) {
       // one launch over all tokens: partials only, or every shard chained in one accumulator
       a.mode = partials_user ? TC_ROWPAR_SHARD : TC_ROWPAR_CHAIN;
@@ -299,9 +313,11 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.y = y + (size_t)m0 * N;
       a.partials = wsP;
       a.pM = mb;
-      a.fold = unfused ? 0 : 1;
+      // the in-kernel fold is done by one CTA per row tile; past a few tokens a separate
+      // fold kernel spread over the whole GPU is faster (both give the same bits)
+      a.fold = (unfused || mb > kTcFoldMaxM) ? 0 : 1;
       if (launch_tc(a, st) != cudaSuccess) return TP_ERR_CUDA;
-      if (unfused && launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
+      if (!a.fold && launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
     }
     return TP_OK;
   }
@@ -355,7 +371,7 @@ bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {
 extern "C" {
 
 tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const void* x, int32_t M,
-                            void* out, uint32_t flags, void* stream) {
+                            void* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
   if (!desc) return TP_ERR_INVALID_ARG;
   const int kind = desc->kind;
   if (kind != TP_W_GATE_UP && kind != TP_W_QKV) return TP_ERR_INVALID_ARG;
@@ -369,7 +385,10 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   if (M == 0) return TP_OK;
   if (!aligned16(x) || !aligned16(out)) return TP_ERR_ALIGN;
   const int mode = kind == TP_W_GATE_UP ? COLPAR_SWIGLU : (f32 ? COLPAR_F32 : COLPAR_BF16);
-  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags);
+  void* sk_ws = nullptr;  // optional stream-K scratch: the tail of a tp_workspace_bytes() workspace
+  const uint64_t off = partials_bytes(desc->shape.t, M, desc->shape.d) + ticket_bytes(desc->shape.d);
+  if (ws && aligned16(ws) && ws_bytes >= off + tc_streamk_bytes()) sk_ws = static_cast<uint8_t*>(ws) + off;
+  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags, sk_ws);
 }
 
 tp_status tp_rowpar_partials(const tp_packed_desc* desc, const void* w, const void* a, int32_t M,
@@ -431,7 +450,8 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
     return TP_ERR_ALIGN;
   if (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
-  st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags);
+  st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags,
+                  static_cast<uint8_t*>(ws) + partials_bytes(gu->shape.t, M, gu->shape.d) + ticket_bytes(gu->shape.d));
   if (st != TP_OK) return st;
   return run_rowpar(dn, dn_w, static_cast<const bf16*>(h_out), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
@@ -456,7 +476,8 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
   const tp_shape& sh = qkv->shape;
   if (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
-  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags);
+  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags,
+                  static_cast<uint8_t*>(ws) + partials_bytes(sh.t, M, sh.d) + ticket_bytes(sh.d));
   if (st != TP_OK) return st;
   st = cuda_status(launch_attn1(static_cast<const bf16*>(qkv_out), M, sh.n_q_heads, sh.n_kv_heads,
                                 sh.head_dim, sh.t, static_cast<bf16*>(o_in), s));
@@ -502,7 +523,7 @@ tp_status tp_sync(void* stream, int32_t timeout_ms) {
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = 16u << 20;  // 16 MiB
+constexpr size_t kNoallocScratchBytes = 32u << 20;  // 32 MiB
 static __device__ __align__(256) unsigned char tpx_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_noalloc_mu;
@@ -541,13 +562,16 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   if (M == 0) return TP_OK;
   if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
   const int t = desc->shape.t, N = (int)desc->rows_per_shard;
-  const uint64_t pb = partials_bytes(t, M, N), need = pb + ticket_bytes(N);
+  const uint64_t pb = partials_bytes(t, M, N), need = pb + ticket_bytes(N) + tc_streamk_bytes();
   if (need > kNoallocScratchBytes) return TP_ERR_WORKSPACE;  // beyond the static scratch
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != TP_OK) return st;
   // the tickets must start at zero; the partials are fully written before they are read
-  if (cudaMemsetAsync(static_cast<uint8_t*>(scratch) + pb, 0, ticket_bytes(N), S(stream)) != cudaSuccess)
+  uint8_t* sc = static_cast<uint8_t*>(scratch);
+  if (cudaMemsetAsync(sc + pb, 0, ticket_bytes(N), S(stream)) != cudaSuccess ||
+      cudaMemsetAsync(sc + need - (size_t)kTcMaxStreamkItems * 4, 0, (size_t)kTcMaxStreamkItems * 4,
+                      S(stream)) != cudaSuccess)
     return TP_ERR_CUDA;
   return run_rowpar(desc, w, static_cast<const bf16*>(a), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, scratch, (size_t)need, flags, S(stream));

@@ -85,6 +85,51 @@ __device__ __forceinline__ void decode_item(const TcArgs& a, const Geo& g, int i
   }
 }
 
+// Work of one CTA: whole items strided over the grid, or (stream-K) an equal contiguous
+// share of the flattened (item, k-block) space, cut into segments at item boundaries.
+struct Seg {
+  int item, kb_lo, kb_hi;
+};
+
+struct SegIter {
+  bool sk;
+  int nkb, n_items, G, item;
+  long long cur, end;
+  __device__ SegIter(bool streamk, const Geo& g)
+      : sk(streamk), nkb(g.nkb), n_items(g.n_items), G(gridDim.x), item(blockIdx.x), cur(0), end(0) {
+    if (sk) {
+      const long long total = (long long)n_items * nkb;
+      cur = total * blockIdx.x / G;
+      end = total * (blockIdx.x + 1) / G;
+    }
+  }
+  __device__ bool next(Seg& sg) {
+    if (!sk) {
+      if (item >= n_items) return false;
+      sg = {item, 0, nkb};
+      item += G;
+      return true;
+    }
+    if (cur >= end) return false;
+    sg.item = (int)(cur / nkb);
+    sg.kb_lo = (int)(cur % nkb);
+    const long long rem = end - cur;
+    sg.kb_hi = rem < (long long)(nkb - sg.kb_lo) ? sg.kb_lo + (int)rem : nkb;
+    cur += sg.kb_hi - sg.kb_lo;
+    return true;
+  }
+};
+
+__device__ __forceinline__ long long share_start(long long total, int G, int c) { return total * c / G; }
+
+// CTA whose stream-K share contains flattened k-block x.
+__device__ __forceinline__ int share_owner(long long total, int G, long long x) {
+  int c = (int)(x * G / total);
+  while (c > 0 && share_start(total, G, c) > x) --c;
+  while (c + 1 < G && share_start(total, G, c + 1) <= x) ++c;
+  return c;
+}
+
 __device__ __forceinline__ void raise_error(unsigned code, volatile int* abort_flag) {
   atomicExch(&g_tc_error, code);
   *abort_flag = 1;
@@ -171,6 +216,60 @@ __device__ bool rowpar_fold(const TcArgs& a, const Geo& g, int rt, int tt, int p
   return true;
 }
 
+// A CTA that stored one piece of an item: the last of the item's pieces to arrive sums all
+// pieces in k order (piece of CTA c_a first) and runs the item's epilogue.  *done = 1 there.
+template <int BN>
+__device__ bool streamk_complete(const TcArgs& a, const Geo& g, const Seg& sg, int s, int p, int m0,
+                                 uint32_t epi_bar, int& phase, volatile int* last_flag,
+                                 volatile int* abort_flag, int* done) {
+  const int G = gridDim.x;
+  const long long total = (long long)g.n_items * g.nkb, istart = (long long)sg.item * g.nkb;
+  const int ca = share_owner(total, G, istart), cb = share_owner(total, G, istart + g.nkb - 1);
+  __threadfence();
+  mbar_arrive(epi_bar);
+  if (!mbar_wait(epi_bar, phase)) {
+    raise_error(9, abort_flag);
+    return false;
+  }
+  phase ^= 1;
+  if (threadIdx.x == 0) {
+    int pieces = 0;  // CTAs between ca and cb with a non-empty share (all of them when G <= total)
+    for (int c = ca; c <= cb; ++c) pieces += share_start(total, G, c + 1) > share_start(total, G, c);
+    const unsigned old = atomicAdd(&a.item_tickets[sg.item], 1u);
+    *last_flag = old == (unsigned)(pieces - 1);
+  }
+  mbar_arrive(epi_bar);
+  if (!mbar_wait(epi_bar, phase)) {
+    raise_error(10, abort_flag);
+    return false;
+  }
+  phase ^= 1;
+  *done = *last_flag;
+  if (!*done) return true;
+  __threadfence();
+  const int r = threadIdx.x;
+#pragma unroll 1
+  for (int c0 = 0; c0 < BN; c0 += 16) {
+    float v[16];
+    bool first = true;
+#pragma unroll 1
+    for (int c = ca; c <= cb; ++c) {
+      if (share_start(total, G, c + 1) == share_start(total, G, c)) continue;  // empty share
+      const int slot = share_start(total, G, c) < istart ? 1 : 0;
+      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM + (size_t)c0 * BM + r;
+      float w[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[j] = __ldcg(src + j * BM);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = first ? w[j] : v[j] + w[j];
+      first = false;
+    }
+    epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+  }
+  if (threadIdx.x == 0) a.item_tickets[sg.item] = 0u;
+  return true;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
@@ -225,13 +324,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     if (lane == 0) {
-      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x) {
+      SegIter segs(a.streamk != 0, g);
+      Seg sg;
+      bool ok = true;
+      while (ok && !*abort_flag && segs.next(sg)) {
         int s, rt, tt;
-        decode_item(a, g, item, s, rt, tt);
-        for (int kb = 0; kb < g.nkb; ++kb) {
+        decode_item(a, g, sg.item, s, rt, tt);
+        for (int kb = sg.kb_lo; kb < sg.kb_hi; ++kb) {
           const int st = issued % S;
           if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
             raise_error(1, abort_flag);
+            ok = false;
             break;
           }
           const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
@@ -248,7 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(BM, BN);
       int consumed = 0, it = 0;
-      for (int item = blockIdx.x; item < g.n_items && !*abort_flag; item += gridDim.x, ++it) {
+      SegIter segs(a.streamk != 0, g);
+      Seg sg;
+      while (!*abort_flag && segs.next(sg)) {
         const int acc = it & 1;
         if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) {
           raise_error(2, abort_flag);
@@ -257,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
-        for (int kb = 0; kb < g.nkb; ++kb) {
+        for (int kb = sg.kb_lo; kb < sg.kb_hi; ++kb) {
           const int st = consumed % S;
           if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1)) {
             raise_error(3, abort_flag);
@@ -268,12 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)st * C::kBBytes);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb | k) != 0);
+            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > sg.kb_lo) || k != 0);
           mma_commit(empty0 + 8 * st);  // the stage is free once these MMAs have read it
           ++consumed;
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);   // accumulator ready for the epilogue
+        ++it;
       }
       *mma_consumed = consumed;
       // wait for every MMA this thread issued before the TMEM can be released
@@ -284,10 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue warps 0..3
     const int r = warp * 32 + lane;  // row inside the 128-row tile
     int it = 0, epi_phase = 0;
-    for (int item = blockIdx.x; item < g.n_items; item += gridDim.x, ++it) {
+    SegIter segs(a.streamk != 0, g);
+    Seg sg;
+    while (segs.next(sg)) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       int s, rt, tt;
-      decode_item(a, g, item, s, rt, tt);
+      decode_item(a, g, sg.item, s, rt, tt);
       const int acc = it & 1;
       // warp-uniform: the tcgen05.ld below is a warp-collective instruction
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
@@ -298,17 +406,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
       const int p = rt * BM + r;  // row of the shard's matrix
       const int m0 = tt * BN;
+      const bool whole = sg.kb_lo == 0 && sg.kb_hi == g.nkb;
+      float* piece = nullptr;
+      if (!whole) {  // this CTA holds one piece of the item: stash it as [col][row]
+        const long long total = (long long)g.n_items * g.nkb, istart = (long long)sg.item * g.nkb;
+        const int slot = share_start(total, gridDim.x, blockIdx.x) < istart ? 1 : 0;
+        piece = a.pieces + ((size_t)blockIdx.x * 2 + slot) * BN * BM;
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(tb + c0, v);
         tmem_ld_wait();
-        epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+        if (whole) {
+          epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) piece[(c0 + j) * BM + r] = v[j];
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (a.mode == TC_ROWPAR_SHARD && a.fold) {
+      ++it;
+      bool complete = whole;
+      if (!whole) {
+        int done = 0;
+        if (!streamk_complete<BN>(a, g, sg, s, p, m0, epi_bar, epi_phase, last_flag, abort_flag, &done)) break;
+        complete = done != 0;
+      }
+      if (complete && a.mode == TC_ROWPAR_SHARD && a.fold) {
         if (!rowpar_fold<BN>(a, g, rt, tt, p, epi_bar, epi_phase, last_flag, abort_flag)) break;
       }
     }
@@ -401,8 +528,13 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st) {
   }
   const int n_rt = a.rows / BM, n_tt = (a.M + BN - 1) / BN;
   const int n_items = a.mode == TC_ROWPAR_CHAIN ? n_rt * n_tt : n_rt * n_tt * a.t;
-  const int grid = n_items < sm_count() ? n_items : sm_count();
-  tc_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(tmA, tmB, a);
+  const int sms = sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid;
+  TcArgs b = a;
+  // stream-K when the caller gave scratch for it and the tokens fit one decode tile
+  b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items <= kTcMaxStreamkItems;
+  const long long total_kb = (long long)n_items * (a.mode == TC_ROWPAR_CHAIN ? a.K / BK * a.t : a.K / BK);
+  const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);
+  tc_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(tmA, tmB, b);
   note_launch();
   return cudaGetLastError();
 }

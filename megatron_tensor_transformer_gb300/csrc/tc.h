@@ -31,7 +31,20 @@ struct TcArgs {
   int pM;
   unsigned* tickets;              // one per (row tile, token tile), zero between launches
   int fold;                       // TC_ROWPAR_SHARD: 1 = last shard folds into y, 0 = partials only
+  // stream-K (decode token tiles): pieces of items cut across CTAs are summed in k order by
+  // the CTA that finishes an item last
+  int streamk;
+  float* pieces;                  // [grid][2][BN][128] fp32
+  unsigned* item_tickets;         // one per item, zero between launches
 };
+
+constexpr int kTcMaxGrid = 160;          // persistent CTAs (capped so workspace sizes are fixed)
+constexpr int kTcMaxStreamkItems = 4096;
+constexpr int kTcStreamkMaxBN = 64;
+// bytes of stream-K scratch (pieces + item tickets) for token tile BN
+inline size_t tc_streamk_bytes() {
+  return (size_t)kTcMaxGrid * 2 * kTcStreamkMaxBN * 128 * 4 + (size_t)kTcMaxStreamkItems * 4;
+}
 
 // Whether the tcgen05 path supports this geometry (rows % 128, K % 64, bf16 weights).
 bool tc_supported(int rows, int K, bool fp8);

@@ -64,7 +64,7 @@ def lib():
             "tp_mlp_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, V, V, I32, V, V, V, SZ, U32, V]),
             "tp_proj_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, V, V, I32, V, V, V, V, SZ, U32, V]),
             "tp_reduce_partials": (I32, [V, I32, I32, I32, V, V, V]),
-            "tp_colpar_forward": (I32, [P(PackedDesc), V, V, I32, V, U32, V]),
+            "tp_colpar_forward": (I32, [P(PackedDesc), V, V, I32, V, V, SZ, U32, V]),
             "tp_rowpar_partials": (I32, [P(PackedDesc), V, V, I32, V, V]),
             "tp_rowpar_forward": (I32, [P(PackedDesc), V, V, V, I32, V, V, SZ, U32, V]),
             "tp_rowpar_forward_noalloc": (I32, [P(PackedDesc), V, V, V, I32, V, U32, V]),
@@ -163,9 +163,9 @@ def tp_reduce_partials(partials, t, M, d, residual, y, stream=None):
     return y
 
 
-def tp_colpar_forward(desc, w, x, out, flags=0, stream=None):
-    _check(lib().tp_colpar_forward(ctypes.byref(desc), _ptr(w), _ptr(x), x.shape[0], _ptr(out), flags,
-                                   _stream(stream)), "tp_colpar_forward")
+def tp_colpar_forward(desc, w, x, out, flags=0, stream=None, ws=None):
+    _check(lib().tp_colpar_forward(ctypes.byref(desc), _ptr(w), _ptr(x), x.shape[0], _ptr(out), _ptr(ws),
+                                   0 if ws is None else ws.numel(), flags, _stream(stream)), "tp_colpar_forward")
     return out
 
 

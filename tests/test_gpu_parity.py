@@ -89,8 +89,8 @@ class Mlp:
 
     def run(self, residual=True, flags=0, x=None):
         x = self.x if x is None else x
-        y = torch.empty_like(x)
-        h = torch.empty((x.shape[0], self.ffn), dtype=torch.bfloat16, device=self.dev)
+        y = torch.full_like(x, float("nan"))          # poisoned: unwritten outputs show up
+        h = torch.full((x.shape[0], self.ffn), float("nan"), dtype=torch.bfloat16, device=self.dev)
         tpx.tp_mlp_forward(self.gu, self.gu_w, self.dn, self.dn_w, x, x if residual else None, y, h,
                            self.ws, flags)
         torch.cuda.synchronize()
@@ -183,7 +183,7 @@ def test_colpar_qkv_exact_on_integers_and_t_invariant(dev, t):
     w = inputs.small_int_bf16((d, (n_q + 2 * n_kv) * hd), -2, 2, 1, 2, dev)
     sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
     q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, w)
-    out = torch.empty((M, (n_q + 2 * n_kv) * hd), dtype=torch.float32, device=dev)
+    out = torch.full((M, (n_q + 2 * n_kv) * hd), float("nan"), dtype=torch.float32, device=dev)
     tpx.tp_colpar_forward(q, q_w, x, out, flags=tpx.TP_F_FP32_COLPAR_OUT)
     torch.cuda.synchronize()
     full = O.as_f64(bits(x)) @ O.as_f64(bits(w))
@@ -199,9 +199,9 @@ def test_rowpar_partials_and_fold_exact_on_integers(dev, t):
     res = inputs.small_int_bf16((M, d), -4, 4, 2, 3, dev)
     sh = tpx.make_shape(d, ffn=ffn, t=t)
     w_p, desc = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, w)
-    P = torch.empty((t, M, d), dtype=torch.float32, device=dev)
+    P = torch.full((t, M, d), float("nan"), dtype=torch.float32, device=dev)
     tpx.tp_rowpar_partials(desc, w_p, a, P)
-    y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=dev)
     tpx.tp_reduce_partials(P, t, M, d, res, y)
     torch.cuda.synchronize()
     af, wf = O.as_f64(bits(a)), O.as_f64(bits(w))
@@ -222,7 +222,7 @@ def test_reduce_fold_order_is_left_to_right(dev):
     for s in range(t):
         P[s] = vals[(s + rng.integers(0, 8, size=(M, d))) % 8] * rng.choice([1, -1], size=(M, d))
     res = inputs.normal_bf16((M, d), 1.0, 3, 9, dev)
-    y = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=dev)
     tpx.tp_reduce_partials(torch.from_numpy(P).to(dev), t, M, d, res, y)
     torch.cuda.synchronize()
     acc = P[0].copy()
@@ -327,9 +327,9 @@ def run_proj(d, n_q, n_kv, hd, t, M, dev, seed=0, residual=True, flags=0):
     q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv)
     o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo)
     Q = (n_q + 2 * n_kv) * hd
-    y = torch.empty_like(x)
-    qkv = torch.empty((M, Q), dtype=torch.bfloat16, device=dev)
-    o_in = torch.empty((M, n_q * hd), dtype=torch.bfloat16, device=dev)
+    y = torch.full_like(x, float("nan"))
+    qkv = torch.full((M, Q), float("nan"), dtype=torch.bfloat16, device=dev)
+    o_in = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = tpx.new_workspace(sh, M, dev)
     tpx.tp_proj_forward(q, q_w, o, o_w, x, x if residual else None, y, qkv, o_in, ws, flags)
     torch.cuda.synchronize()
@@ -357,7 +357,7 @@ def test_proj_small_ragged(dev):
 @pytest.mark.parametrize("M,d", [(16, 16384), (3, 256), (1, 8192)])
 def test_rmsnorm(dev, M, d):
     x = inputs.normal_bf16((M, d), 1.5, 0, 21, dev)
-    out = torch.empty_like(x)
+    out = torch.full_like(x, float("nan"))
     tpx.tp_rmsnorm(x, out, 1e-5)
     torch.cuda.synchronize()
     ref = O.rmsnorm(bits(x), 1e-5)

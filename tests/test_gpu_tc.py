@@ -24,15 +24,19 @@ def dev():
     return torch.device("cuda:0")
 
 
+@pytest.mark.parametrize("with_ws", [False, True])
 @pytest.mark.parametrize("t,M", [(8, 19), (1, 5), (2, 64), (4, 130), (8, 300)])
-def test_tc_colpar_exact_on_integers(dev, t, M):
+def test_tc_colpar_exact_on_integers(dev, t, M, with_ws):
+    """With a workspace the kernel may cut items across CTAs (stream-K); the pieces must
+    still sum to the exact product."""
     d, n_q, n_kv, hd = 256, 16, 8, 32
     x = inputs.small_int_bf16((M, d), -2, 2, 1, 1, dev)
     w = inputs.small_int_bf16((d, (n_q + 2 * n_kv) * hd), -2, 2, 1, 2, dev)
     sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
     q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, w)
-    out = torch.empty((M, (n_q + 2 * n_kv) * hd), dtype=torch.float32, device=dev)
-    tpx.tp_colpar_forward(q, q_w, x, out, flags=tpx.TP_F_FP32_COLPAR_OUT | TC)
+    out = torch.full((M, (n_q + 2 * n_kv) * hd), float("nan"), dtype=torch.float32, device=dev)
+    ws = tpx.new_workspace(sh, M, dev) if with_ws else None
+    tpx.tp_colpar_forward(q, q_w, x, out, flags=tpx.TP_F_FP32_COLPAR_OUT | TC, ws=ws)
     assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
     full = O.as_f64(bits(x)) @ O.as_f64(bits(w))
     cols = np.concatenate([O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0] for s in range(t)])
@@ -113,3 +117,21 @@ def test_tc_and_skinny_both_within_bar(dev):
     for f in (TC, SK):
         y, _ = m.run(flags=f)
         check_close(bits(y), y_ref, what=f"flags={f}")
+
+
+@pytest.mark.parametrize("t,M", [(8, 64), (8, 16), (1, 32)])
+def test_tc_streamk_rowpar_exact_on_integers(dev, t, M):
+    """Row-parallel through the fused entry point (stream-K pieces, then the shard fold) on
+    integers: the result is exact, so every piece and every shard must be summed once."""
+    d, ffn = 1024, 8192
+    a = inputs.small_int_bf16((M, ffn), -1, 1, 5, 1, dev)
+    w = inputs.small_int_bf16((ffn, d), -1, 1, 5, 2, dev)
+    res = inputs.small_int_bf16((M, d), -4, 4, 5, 3, dev)
+    sh = tpx.make_shape(d, ffn=ffn, t=t)
+    w_p, desc = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, w)
+    ws = tpx.new_workspace(sh, M, dev)
+    y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    tpx.tp_rowpar_forward(desc, w_p, a, res, y, ws, flags=TC)
+    assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
+    exact = O.as_f64(bits(a)) @ O.as_f64(bits(w)) + O.as_f64(bits(res))
+    assert np.array_equal(bits(y), O.f64_to_bf16_bits(exact))

@@ -58,9 +58,9 @@ def test_noalloc_matches_workspace_entry_point_twice(dev, d, ffn, t, M, flags):
 
 def test_noalloc_rejects_requests_beyond_its_scratch(dev):
     cap = tpx.tp_noalloc_scratch_capacity()
-    assert cap == 16 << 20
-    # 70B-shaped o_proj at 64 tokens needs 8 * 64 * 8192 * 4 bytes of partials: 16 MiB + tickets
-    sh = tpx.make_shape(8192, n_q=64, n_kv=8, hd=128, t=8)
+    assert cap == 32 << 20
+    # 405B-shaped o_proj at 64 tokens needs 8 * 64 * 16384 * 4 bytes of partials: 32 MiB + more
+    sh = tpx.make_shape(16384, n_q=128, n_kv=8, hd=128, t=8)
     desc = tpx.tp_describe(sh, tpx.TP_W_O)
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the size check fails first
     st = tpx.lib().tp_rowpar_forward_noalloc(ctypes.byref(desc), fake, fake, None, 64, fake, 0, None)
