@@ -249,12 +249,16 @@ def run_tpx(args, rank, world, local):
                 os.path.join(ROOT, "gpurun_out")) else f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
             t_start.record(stream)
             for i in range(K):
-                step(i)
+                step()          # no events between kernels: consecutive kernels may overlap
             t_end.record(stream)
             t_end.synchronize()
         launches = tpx.tp_launch_count() - n0
         torch.cuda.synchronize()
         barrier(world)
+        # second pass, same work, with an event around every kernel: per-kernel durations
+        for i in range(K):
+            step(i)
+        torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end)
     ms_max = max_over_ranks(ms, world, dev)
     per_M = {}

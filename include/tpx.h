@@ -96,6 +96,12 @@ typedef struct {
 #define TP_F_UNFUSED_REDUCE 0x1u  /* row-parallel: write shard partials to the workspace, then
                                      run tp_reduce_partials (same bits as the fused path) */
 #define TP_F_FP32_COLPAR_OUT 0x2u /* tp_colpar_forward: write fp32 instead of bf16 */
+#define TP_F_SERIAL 0x40u         /* launch every kernel only after the previous work on the stream has
+                                     finished.  By default a forward's tcgen05 kernels start streaming
+                                     weights while the previous kernel drains (programmatic dependent
+                                     launch): packed weights must then not be written by work still in
+                                     flight on the stream (tp_partition_weights returns with them
+                                     complete).  Activations are always read after earlier work ends. */
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernel (bf16 weights, rows % 128, K % 64);
                                      default: tcgen05 where supported for M > 16, else mma.sync */
@@ -111,7 +117,8 @@ tp_status tp_describe(const tp_shape* shape /* host */, int32_t kind, tp_packed_
  * "RowParallelLinear", scalablesystem.dev).  W0: [in,out] bf16 (W_gate for GATE_UP);
  * W1: W_up for GATE_UP, else NULL.  packed: packed_bytes >= tp_packed_bytes().
  * Writes the layout described above; for FP8 also quantises (shape.wtype).  Fills
- * *desc_out (host).  Stream-ordered; W0/W1 may be freed after the stream reaches it. */
+ * *desc_out (host).  Synchronises `stream` before returning, so the packed buffer is
+ * complete (forwards may start reading it early, see TP_F_SERIAL). */
 tp_status tp_partition_weights(const tp_shape* shape /* host */, int32_t kind, const void* W0,
                                const void* W1, void* packed, size_t packed_bytes,
                                tp_packed_desc* desc_out /* host */, void* stream);

@@ -173,6 +173,9 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
   g.shard_stride = d.shard_stride_bytes;
   g.scales_offset = d.scales_offset;
   st = cuda_status(launch_pack(g, static_cast<uint8_t*>(packed), S(stream)));
+  // forwards may start reading weights before earlier work on their stream has finished
+  // (programmatic dependent launch), so the packed buffer is complete when this returns
+  if (st == TP_OK) st = cuda_status(cudaStreamSynchronize(S(stream)));
   if (st == TP_OK) *desc_out = d;
   return st;
 }
@@ -196,6 +199,7 @@ using bf16 = __nv_bfloat16;
 constexpr int kTcMinM = 16;
 constexpr int kTcFoldMaxM = 16;  // tcgen05 row-parallel: fold in the kernel up to this many tokens
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
+constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
@@ -235,7 +239,7 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     a.out = out;
     a.ldo = ldo;
     set_streamk(a, sk_ws);
-    return launch_tc(a, st) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
   }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
     ColparArgs a{};
@@ -302,7 +306,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.partials = partials_user;
       a.pM = M;
       a.fold = 0;
-      return launch_tc(a, st) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+      return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
     }
     for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {  // per-shard partials in the workspace
       const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
@@ -316,7 +320,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       // the in-kernel fold is done by one CTA per row tile; past a few tokens a separate
       // fold kernel spread over the whole GPU is faster (both give the same bits)
       a.fold = (unfused || mb > kTcFoldMaxM) ? 0 : 1;
-      if (launch_tc(a, st) != cudaSuccess) return TP_ERR_CUDA;
+      if (launch_tc(a, st, (flags & TP_F_SERIAL) == 0) != cudaSuccess) return TP_ERR_CUDA;
       if (!a.fold && launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
     }
     return TP_OK;
@@ -378,7 +382,7 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
   if (M < 0 || (M > 0 && (!x || !out))) return TP_ERR_INVALID_ARG;
-  if ((flags & ~(uint32_t)(TP_F_FP32_COLPAR_OUT | kKernelFlags)) || bad_kernel_flags(flags))
+  if ((flags & ~(uint32_t)(TP_F_FP32_COLPAR_OUT | kKernelFlags | TP_F_SERIAL)) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   const bool f32 = (flags & TP_F_FP32_COLPAR_OUT) != 0;
   if (f32 && kind == TP_W_GATE_UP) return TP_ERR_INVALID_ARG;
@@ -413,7 +417,7 @@ tp_status tp_rowpar_forward(const tp_packed_desc* desc, const void* w, const voi
   if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
-  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+  if ((flags & ~kFwdFlags) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
@@ -442,7 +446,7 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
   st = check_desc(dn, TP_W_DOWN, dn_w);
   if (st != TP_OK) return st;
   if (!same_block(gu->shape, dn->shape, true)) return TP_ERR_LAYOUT_MISMATCH;
-  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+  if ((flags & ~kFwdFlags) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!x || !y || !h_out))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
@@ -466,7 +470,7 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
   st = check_desc(o, TP_W_O, o_w);
   if (st != TP_OK) return st;
   if (!same_block(qkv->shape, o->shape, false)) return TP_ERR_LAYOUT_MISMATCH;
-  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+  if ((flags & ~kFwdFlags) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!x || !y || !qkv_out || !o_in))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
@@ -556,7 +560,7 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   if (kind != TP_W_DOWN && kind != TP_W_O) return TP_ERR_INVALID_ARG;
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
-  if ((flags & ~(uint32_t)(TP_F_UNFUSED_REDUCE | kKernelFlags)) || bad_kernel_flags(flags))
+  if ((flags & ~kFwdFlags) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;

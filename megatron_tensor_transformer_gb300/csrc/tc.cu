@@ -322,15 +322,45 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   int issued = 0;  // producer: k-blocks issued
 
+  griddep_launch_dependents();
   if (warp == kProducerWarp) {
     if (lane == 0) {
+      // The packed weights are not written by the kernel this one may overlap with (under
+      // programmatic dependent launch), so the first stages' weight tiles are requested
+      // before waiting on it; the activation tiles only after.
+      int pre = 0, pre_xcol[S], pre_row[S];
+      {
+        SegIter ps(a.streamk != 0, g);
+        Seg q;
+        while (pre < S && ps.next(q)) {
+          int s, rt, tt;
+          decode_item(a, g, q.item, s, rt, tt);
+          for (int kb = q.kb_lo; kb < q.kb_hi && pre < S; ++kb) {
+            const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
+            const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
+            pre_xcol[pre] = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
+            pre_row[pre] = tt * BN;
+            mbar_expect_tx(full0 + 8 * pre, C::kABytes);  // stage `pre` is fresh: no empty wait
+            tma_load_3d(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre);
+            ++pre;
+          }
+        }
+      }
+      griddep_wait();
+      for (int j = 0; j < pre; ++j) {
+        mbar_arrive_expect_tx(full0 + 8 * j, C::kBBytes);
+        tma_load_2d(smem_u32(sB + (size_t)j * C::kBBytes), &tmB, pre_xcol[j], pre_row[j], full0 + 8 * j);
+      }
+      issued = pre;
       SegIter segs(a.streamk != 0, g);
       Seg sg;
       bool ok = true;
+      int seq = 0;
       while (ok && !*abort_flag && segs.next(sg)) {
         int s, rt, tt;
         decode_item(a, g, sg.item, s, rt, tt);
         for (int kb = sg.kb_lo; kb < sg.kb_hi; ++kb) {
+          if (seq++ < pre) continue;  // already issued above
           const int st = issued % S;
           if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
             raise_error(1, abort_flag);
@@ -387,7 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(drain_bar, 0)) raise_error(4, abort_flag);
     }
   } else {
-    // epilogue warps 0..3
+    // epilogue warps 0..3: every global write comes after the grids this one depends on
+    griddep_wait();
     const int r = warp * 32 + lane;  // row inside the 128-row tile
     int it = 0, epi_phase = 0;
     SegIter segs(a.streamk != 0, g);
@@ -497,7 +528,7 @@ unsigned tc_take_device_error() {
 }
 
 template <int BN>
-static cudaError_t tc_go(const TcArgs& a, cudaStream_t st) {
+static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   using C = TcCfg<BN>;
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
@@ -534,19 +565,29 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st) {
   b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items <= kTcMaxStreamkItems;
   const long long total_kb = (long long)n_items * (a.mode == TC_ROWPAR_CHAIN ? a.K / BK * a.t : a.K / BK);
   const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);
-  tc_kernel<BN><<<grid, kThreads, C::kSmem, st>>>(tmA, tmB, b);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN>, tmA, tmB, b);
   note_launch();
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_tc(const TcArgs& a, cudaStream_t st) {
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl) {
   if (!tc_supported(a.rows, a.K, false) || a.M <= 0) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x)) & 15) return cudaErrorInvalidValue;
-  if (a.M <= 16) return tc_go<16>(a, st);
-  if (a.M <= 32) return tc_go<32>(a, st);
-  if (a.M <= 64) return tc_go<64>(a, st);
-  if (a.M <= 128) return tc_go<128>(a, st);
-  return tc_go<256>(a, st);
+  if (a.M <= 16) return tc_go<16>(a, st, pdl);
+  if (a.M <= 32) return tc_go<32>(a, st, pdl);
+  if (a.M <= 64) return tc_go<64>(a, st, pdl);
+  if (a.M <= 128) return tc_go<128>(a, st, pdl);
+  return tc_go<256>(a, st, pdl);
 }
 
 }  // namespace tpx

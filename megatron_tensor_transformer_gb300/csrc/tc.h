@@ -50,7 +50,9 @@ inline size_t tc_streamk_bytes() {
 bool tc_supported(int rows, int K, bool fp8);
 // Ticket slots TC_ROWPAR_SHARD needs for (rows, M).
 int tc_ticket_slots(int rows, int M);
-cudaError_t launch_tc(const TcArgs& a, cudaStream_t st);
+// pdl: launch as a programmatic dependent of the previous kernel on the stream (the weight
+// tiles stream in while that kernel finishes; activations are read after it completes).
+cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl);
 // Device error word set by a bounded wait that gave up (0 = none); read and cleared.
 unsigned tc_take_device_error();
 
