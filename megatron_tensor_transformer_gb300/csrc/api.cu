@@ -197,7 +197,6 @@ using bf16 = __nv_bfloat16;
 // Kernel choice: the tcgen05 GEMM where the geometry allows it and M is above the
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 16;
-constexpr int kTcFoldMaxM = 16;  // tcgen05 row-parallel: fold in the kernel up to this many tokens
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
 constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL;
 
@@ -294,10 +293,10 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     a.K = K;
     a.ldx = K * t;
     a.ldy = N;
-    a.tickets = tickets;
     set_streamk(a, sk_ws);
-    if (partials_user || (!unfused && M > kSkinnyMaxM)) {
-      // one launch over all tokens: partials only, or every shard chained in one accumulator
+    if (partials_user || !unfused) {
+      // one launch over all tokens: per-shard partials only, or (fused) every shard's k-blocks
+      // chained in shard order into one accumulator, + residual: no partials round trip
       a.mode = partials_user ? TC_ROWPAR_SHARD : TC_ROWPAR_CHAIN;
       a.x = a_in;
       a.M = M;
@@ -305,7 +304,6 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.y = y;
       a.partials = partials_user;
       a.pM = M;
-      a.fold = 0;
       return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
     }
     for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {  // per-shard partials in the workspace
@@ -317,11 +315,9 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.y = y + (size_t)m0 * N;
       a.partials = wsP;
       a.pM = mb;
-      // the in-kernel fold is done by one CTA per row tile; past a few tokens a separate
-      // fold kernel spread over the whole GPU is faster (both give the same bits)
-      a.fold = (unfused || mb > kTcFoldMaxM) ? 0 : 1;
+      // unfused: per-shard partials, then the fold kernel
       if (launch_tc(a, st, (flags & TP_F_SERIAL) == 0) != cudaSuccess) return TP_ERR_CUDA;
-      if (!a.fold && launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
+      if (launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
     }
     return TP_OK;
   }

@@ -8,10 +8,9 @@
 // scalablesystem.dev, "The Tensor-Parallel Shard Group") only change which shard buffer
 // and which activation columns a tile reads, and what the epilogue does:
 //   colpar:      store D (or silu(g) * u for interleaved gate/up rows) for shard s;
-//   rowpar:      per-(tile, shard) partial P_s, then the last shard to finish folds
-//                ((P_0 + P_1) + ...) + residual in shard order (Z = sum_k Z_k);
-//   rowpar-chain (large M): all shards' k-blocks accumulate into one TMEM tile in shard
-//                order, + residual (no partials round trip through memory).
+//   rowpar:      per-(tile, shard) partial P_s for the separate shard fold (unfused path);
+//   rowpar-chain (fused): all shards' k-blocks accumulate into one TMEM tile in shard
+//                order, + residual (Z = sum_k Z_k with no partials round trip).
 //
 // Structure: persistent CTAs (one per SM), warp roles:
 //   warps 0-3  epilogue: TMEM -> registers -> global (lane i of warp w = tile row 32w+i)
@@ -177,45 +176,6 @@ __device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, in
   }
 }
 
-// After the t shard partials of (row tile rt, token tile tt) are stored, the last CTA to
-// finish one of them folds ((P_0 + P_1) + ...) + residual into y.  No CTA waits for another.
-template <int BN>
-__device__ bool rowpar_fold(const TcArgs& a, const Geo& g, int rt, int tt, int p, uint32_t epi_bar,
-                            int& phase, volatile int* last_flag, volatile int* abort_flag) {
-  __threadfence();
-  mbar_arrive(epi_bar);
-  if (!mbar_wait(epi_bar, phase)) {
-    raise_error(7, abort_flag);
-    return false;
-  }
-  phase ^= 1;
-  const int slot = rt * g.n_tt + tt;
-  if (threadIdx.x == 0) {
-    const unsigned old = atomicAdd(&a.tickets[slot], 1u);
-    *last_flag = old == (unsigned)(a.t - 1);
-  }
-  mbar_arrive(epi_bar);
-  if (!mbar_wait(epi_bar, phase)) {
-    raise_error(8, abort_flag);
-    return false;
-  }
-  phase ^= 1;
-  if (*last_flag) {
-    __threadfence();
-    const int m1 = min(a.M, (tt + 1) * BN);
-    for (int m = tt * BN; m < m1; ++m) {
-      const size_t pn = (size_t)m * a.rows + p;
-      float v = __ldcg(a.partials + pn);
-      for (int s = 1; s < a.t; ++s) v += __ldcg(a.partials + (size_t)s * a.pM * a.rows + pn);
-      const size_t o = (size_t)m * a.ldy + p;
-      if (a.residual) v += __bfloat162float(a.residual[o]);
-      reinterpret_cast<uint16_t*>(a.y)[o] = f2bf(v);
-    }
-    if (threadIdx.x == 0) a.tickets[slot] = 0u;
-  }
-  return true;
-}
-
 // A CTA that stored one piece of an item: the last of the item's pieces to arrive sums all
 // pieces in k order (piece of CTA c_a first) and runs the item's epilogue.  *done = 1 there.
 template <int BN>
@@ -247,24 +207,30 @@ __device__ bool streamk_complete(const TcArgs& a, const Geo& g, const Seg& sg, i
   *done = *last_flag;
   if (!*done) return true;
   __threadfence();
-  const int r = threadIdx.x;
-#pragma unroll 1
-  for (int c0 = 0; c0 < BN; c0 += 16) {
-    float v[16];
+  if constexpr (BN <= kTcStreamkMaxBN) {
+    // one L2 round trip per piece: all BN values of this thread's row are requested at once
+    const int r = threadIdx.x;
+    float acc[BN];
     bool first = true;
 #pragma unroll 1
     for (int c = ca; c <= cb; ++c) {
       if (share_start(total, G, c + 1) == share_start(total, G, c)) continue;  // empty share
       const int slot = share_start(total, G, c) < istart ? 1 : 0;
-      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM + (size_t)c0 * BM + r;
-      float w[16];
+      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM + r;
+      float w[BN];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) w[j] = __ldcg(src + j * BM);
+      for (int j = 0; j < BN; ++j) w[j] = __ldcg(src + j * BM);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = first ? w[j] : v[j] + w[j];
+      for (int j = 0; j < BN; ++j) acc[j] = first ? w[j] : acc[j] + w[j];
       first = false;
     }
-    epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+#pragma unroll
+    for (int c0 = 0; c0 < BN; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = acc[c0 + j];
+      epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+    }
   }
   if (threadIdx.x == 0) a.item_tickets[sg.item] = 0u;
   return true;
@@ -460,14 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       ++it;
-      bool complete = whole;
       if (!whole) {
         int done = 0;
         if (!streamk_complete<BN>(a, g, sg, s, p, m0, epi_bar, epi_phase, last_flag, abort_flag, &done)) break;
-        complete = done != 0;
-      }
-      if (complete && a.mode == TC_ROWPAR_SHARD && a.fold) {
-        if (!rowpar_fold<BN>(a, g, rt, tt, p, epi_bar, epi_phase, last_flag, abort_flag)) break;
       }
     }
   }
@@ -517,8 +478,6 @@ static int sm_count() {
 }
 
 bool tc_supported(int rows, int K, bool fp8) { return !fp8 && rows % BM == 0 && K % BK == 0 && K > 0; }
-
-int tc_ticket_slots(int rows, int M) { return rows / BM * ((M + 15) / 16); }
 
 unsigned tc_take_device_error() {
   unsigned v = 0, z = 0;

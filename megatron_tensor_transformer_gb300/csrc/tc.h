@@ -10,8 +10,8 @@ enum TcMode {
   TC_COLPAR_BF16 = 0,    // out[m][s*rows + r] = bf16(D)
   TC_COLPAR_F32 = 1,     // same, fp32
   TC_COLPAR_SWIGLU = 2,  // gate/up rows interleaved by 8: out[m][s*rows/2 + f] = bf16(silu(g) u)
-  TC_ROWPAR_SHARD = 3,   // per-(tile, shard) item: partial P_s, then the last shard folds (or not)
-  TC_ROWPAR_CHAIN = 4    // per-tile item: all shards' k chained in one accumulator, + residual
+  TC_ROWPAR_SHARD = 3,   // per-(tile, shard) item: partial P_s (folded afterwards by tp_reduce_partials)
+  TC_ROWPAR_CHAIN = 4    // per-tile item: all shards' k chained in shard order in one accumulator, + residual
 };
 
 struct TcArgs {
@@ -29,8 +29,6 @@ struct TcArgs {
   int ldy;
   float* partials;                // [t][pM][rows]
   int pM;
-  unsigned* tickets;              // one per (row tile, token tile), zero between launches
-  int fold;                       // TC_ROWPAR_SHARD: 1 = last shard folds into y, 0 = partials only
   // stream-K (decode token tiles): pieces of items cut across CTAs are summed in k order by
   // the CTA that finishes an item last
   int streamk;
@@ -48,8 +46,6 @@ inline size_t tc_streamk_bytes() {
 
 // Whether the tcgen05 path supports this geometry (rows % 128, K % 64, bf16 weights).
 bool tc_supported(int rows, int K, bool fp8);
-// Ticket slots TC_ROWPAR_SHARD needs for (rows, M).
-int tc_ticket_slots(int rows, int M);
 // pdl: launch as a programmatic dependent of the previous kernel on the stream (the weight
 // tiles stream in while that kernel finishes; activations are read after it completes).
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl);

@@ -272,15 +272,22 @@ def test_ragged_token_counts(dev, M):
     check_close(bits(y), y_ref, what=f"ragged M={M}")
 
 
-def test_fused_equals_unfused_bitwise_and_deterministic(dev):
+def test_skinny_fused_equals_unfused_bitwise_and_deterministic(dev):
+    """The mma.sync kernel's fused fold (in the CTA, or by the last CTA of a tile) and the
+    unfused partials + fold kernel compute the same per-shard partials and the same left
+    fold, so they give identical bits; every path repeats bit for bit."""
+    sk = tpx.TP_F_KERNEL_SKINNY
     for t, M in [(8, 64), (2, 13), (1, 5)]:
         m = Mlp(4096, 14336, t, M, dev, seed=1)
-        y1, _ = m.run()
-        y2, _ = m.run(flags=tpx.TP_F_UNFUSED_REDUCE)
+        y1, _ = m.run(flags=sk)
+        y2, _ = m.run(flags=sk | tpx.TP_F_UNFUSED_REDUCE)
         assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), (t, M)
         for _ in range(2):
-            y3, _ = m.run()
+            y3, _ = m.run(flags=sk)
             assert torch.equal(y1.view(torch.int16), y3.view(torch.int16)), (t, M)
+            y4, _ = m.run()
+            y5, _ = m.run()
+            assert torch.equal(y4.view(torch.int16), y5.view(torch.int16)), (t, M)
 
 
 def test_zero_tokens_is_a_no_op(dev):
