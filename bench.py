@@ -301,6 +301,101 @@ def run_tpx(args, rank, world, local):
         print(json.dumps(out), flush=True)
 
 
+LAYERS = {
+    # name: (d, ffn, n_q, n_kv, hd, t, M)
+    "70b-layer-decode": (8192, 28672, 64, 8, 128, 8, 32),
+    "70b-layer-prefill": (8192, 28672, 64, 8, 128, 8, 4096),
+}
+
+
+def layer_params(d, ffn, n_q, n_kv, hd):
+    return d * (n_q + 2 * n_kv) * hd + n_q * hd * d + 3 * d * ffn
+
+
+def run_layer(args, rank, world, local):
+    """One 70B-shaped layer's linear parts: y1 = x + o_proj(attn(qkv(x))); y = y1 + MLP(y1),
+    t logical shards, bf16, through tp_proj_forward and tp_mlp_forward.  Decode is reported in
+    tokens/s and HBM GB/s, prefill in TFLOP/s (2 flops per weight per token)."""
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+
+    d, ffn, n_q, n_kv, hd, t, M = LAYERS[args.workload]
+    prefill = "prefill" in args.workload
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
+    _, wg, wu, wd = inputs.mlp_inputs(d, ffn, 1, seed=0, device=dev)
+    gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu, stream=stream)
+    dn_w, dn = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, wd, stream=stream)
+    del wg, wu, wd
+    _, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, 1, seed=0, device=dev)
+    q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv, stream=stream)
+    o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo, stream=stream)
+    del wqkv, wo
+    Q = (n_q + 2 * n_kv) * hd
+    x = inputs.normal_bf16((M, d), 1.0, 0, inputs.STREAM_X, dev)
+    y1, y = torch.empty_like(x), torch.empty_like(x)
+    qkv = torch.empty((M, Q), dtype=torch.bfloat16, device=dev)
+    o_in = torch.empty((M, n_q * hd), dtype=torch.bfloat16, device=dev)
+    h = torch.empty((M, ffn), dtype=torch.bfloat16, device=dev)
+    ws = tpx.new_workspace(sh, M, dev)
+    K = args.steps
+
+    def step():
+        tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y1, qkv, o_in, ws, stream=stream)
+        tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = tpx.tp_launch_count()
+        with Clocks(f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
+            a.record(stream)
+            for _ in range(K):
+                step()
+            b.record(stream)
+            b.synchronize()
+        launches = tpx.tp_launch_count() - n0
+        # dominant kernel alone: the MLP's column-parallel gate/up + SwiGLU
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            tpx.tp_colpar_forward(gu, gu_w, y1, h, stream=stream, ws=ws)
+        c1.record(stream)
+        c1.synchronize()
+    ms = a.elapsed_time(b) / K
+    col_ms = c0.elapsed_time(c1) / K
+    params = layer_params(d, ffn, n_q, n_kv, hd)
+    flops = 2.0 * params * M
+    wbytes = 2.0 * params
+    col_flops, col_bytes = 2.0 * 2 * d * ffn * M, 2.0 * 2 * d * ffn + 2.0 * M * (d + ffn)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "steps": K, "warmup": args.warmup,
+           "ms_per_step": ms, "dtype": "bf16", "data": "synthetic",
+           "config": {"workload": args.workload, "d": d, "ffn": ffn, "n_q": n_q, "n_kv": n_kv,
+                      "head_dim": hd, "t": t, "M": M},
+           "gpu_launches": launches, "clocks": clk.summary()}
+    if prefill:
+        out.update({"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "higher_is_better": True,
+                    "tflop_per_step": flops / 1e12,
+                    "roofline": {"bound": "tensor", "kernel": "tc_kernel (gate/up + SwiGLU)",
+                                 "achieved": col_flops / (col_ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"],
+                                 "unit": "TFLOP/s", "frac": col_flops / (col_ms * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                 "layer_frac": flops / (ms * 1e-3) / 1e12 / pk["bf16_tflops"]}})
+    else:
+        out.update({"value": M / (ms * 1e-3), "unit": "tokens/s", "higher_is_better": True,
+                    "hbm_gbs_step": wbytes / (ms * 1e-3) / 1e9,
+                    "roofline": {"bound": "hbm", "kernel": "tc_kernel (gate/up + SwiGLU)",
+                                 "achieved": col_bytes / (col_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
+                                 "unit": "GB/s", "frac": col_bytes / (col_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                                 "layer_frac": wbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}})
+    print(json.dumps(out), flush=True)
+
+
 def run_e2e(args, gu, gu_w, dn, dn_w, sh, dev):
     """Through the public C-ABI call tp_mlp_forward with HOST buffers: every step copies each
     batch's x from pinned host memory, runs the block, and copies y back."""
@@ -344,13 +439,17 @@ def main():
     ap.add_argument("--impl", default="tpx", choices=["tpx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", default="8b-mlp-decode", choices=["8b-mlp-decode"] + sorted(LAYERS),
+                    help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny"],
                     help="force the tcgen05 or the mma.sync decode kernel (default: library policy)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_setup()
-    if args.impl == "reference":
+    if args.workload != "8b-mlp-decode":
+        run_layer(args, rank, world, local)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_tpx(args, rank, world, local)
