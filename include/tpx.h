@@ -104,7 +104,7 @@ typedef struct {
                                      complete).  Activations are always read after earlier work ends. */
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernel (bf16 weights, rows % 128, K % 64);
-                                     default: tcgen05 where supported for M > 16, else mma.sync */
+                                     default: tcgen05 where supported, else mma.sync */
 
 /* Size in bytes of the packed buffer for (shape, kind); 0 if the shape is invalid. */
 size_t tp_packed_bytes(const tp_shape* shape /* host */, int32_t kind);

@@ -94,6 +94,10 @@ uint64_t partials_bytes(int t, int M, int N) {
   return align_up((uint64_t)t * mb * N * 4);
 }
 uint64_t ticket_bytes(int N) { return align_up((uint64_t)(N / 8 + 1) * 4); }
+// Workspace layout: [stream-K scratch][row-tile tickets][shard partials for min(M, 64) tokens].
+// Everything that must persist between calls (tickets, barrier words) sits at offsets that do
+// not depend on M, so calls with different M can share one workspace.
+uint64_t sk_bytes() { return align_up(tc_streamk_bytes()); }
 
 }  // namespace
 
@@ -183,7 +187,7 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
 size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
   (void)flags;
   if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
-  return (size_t)(partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d) + align_up(tc_streamk_bytes()));
+  return (size_t)(sk_bytes() + partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d));
 }
 
 }  // extern "C"
@@ -196,7 +200,7 @@ using bf16 = __nv_bfloat16;
 
 // Kernel choice: the tcgen05 GEMM where the geometry allows it and M is above the
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
-constexpr int kTcMinM = 16;
+constexpr int kTcMinM = 0;  // tcgen05 wherever the geometry allows: with PDL it wins the whole step
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
 constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL;
 
@@ -208,6 +212,20 @@ bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
 }
 
 bool bad_kernel_flags(uint32_t flags) { return (flags & kKernelFlags) == kKernelFlags; }
+
+int device_sms() {  // cached per device ordinal
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
 
 // Stream-K scratch of the tcgen05 kernel: [pieces][item tickets], or none.
 void set_streamk(TcArgs& a, void* sk_ws) {
@@ -274,16 +292,15 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   const bool need_ws = !partials_user && (unfused || plan.S > 1 || tc);
   float* wsP = nullptr;
   unsigned* tickets = nullptr;
+  void* sk_ws = nullptr;
   if (need_ws) {
     const uint64_t pb = partials_bytes(t, M, N);
-    if (!ws || ws_bytes < pb + ticket_bytes(N)) return TP_ERR_WORKSPACE;
+    if (!ws || ws_bytes < sk_bytes() + pb + ticket_bytes(N)) return TP_ERR_WORKSPACE;
     if (!aligned16(ws)) return TP_ERR_ALIGN;
-    wsP = static_cast<float*>(ws);
-    tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + pb);
+    sk_ws = ws;
+    tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + sk_bytes());
+    wsP = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sk_bytes() + ticket_bytes(N));
   }
-  void* sk_ws = nullptr;
-  if (need_ws && ws_bytes >= partials_bytes(t, M, N) + ticket_bytes(N) + tc_streamk_bytes())
-    sk_ws = static_cast<uint8_t*>(ws) + partials_bytes(t, M, N) + ticket_bytes(N);
   if (tc) {
     TcArgs a{};
     a.w = static_cast<const uint8_t*>(w);
@@ -294,9 +311,13 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     a.ldx = K * t;
     a.ldy = N;
     set_streamk(a, sk_ws);
-    if (partials_user || !unfused) {
-      // one launch over all tokens: per-shard partials only, or (fused) every shard's k-blocks
-      // chained in shard order into one accumulator, + residual: no partials round trip
+    // Fused default: chain every shard's k-blocks into one accumulator (no partials round
+    // trip) when its row tiles fill the GPU; otherwise (decode: few 128-row tiles) per-shard
+    // items, which do fill it, then the fold kernel over the partials.
+    const int tiles = N / 128 * ((M + 255) / 256), sms = device_sms();
+    const bool fold_pass = !partials_user && (unfused || (M <= kSkinnyMaxM && tiles < sms && tiles * t >= sms));
+    if (!fold_pass) {
+      // one launch over all tokens: per-shard partials only, or every shard chained, + residual
       a.mode = partials_user ? TC_ROWPAR_SHARD : TC_ROWPAR_CHAIN;
       a.x = a_in;
       a.M = M;
@@ -385,9 +406,8 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   if (M == 0) return TP_OK;
   if (!aligned16(x) || !aligned16(out)) return TP_ERR_ALIGN;
   const int mode = kind == TP_W_GATE_UP ? COLPAR_SWIGLU : (f32 ? COLPAR_F32 : COLPAR_BF16);
-  void* sk_ws = nullptr;  // optional stream-K scratch: the tail of a tp_workspace_bytes() workspace
-  const uint64_t off = partials_bytes(desc->shape.t, M, desc->shape.d) + ticket_bytes(desc->shape.d);
-  if (ws && aligned16(ws) && ws_bytes >= off + tc_streamk_bytes()) sk_ws = static_cast<uint8_t*>(ws) + off;
+  void* sk_ws = nullptr;  // optional stream-K scratch: the head of a tp_workspace_bytes() workspace
+  if (ws && aligned16(ws) && ws_bytes >= sk_bytes()) sk_ws = ws;
   return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags, sk_ws);
 }
 
@@ -451,7 +471,7 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
   if (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
   st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags,
-                  static_cast<uint8_t*>(ws) + partials_bytes(gu->shape.t, M, gu->shape.d) + ticket_bytes(gu->shape.d));
+                  ws);
   if (st != TP_OK) return st;
   return run_rowpar(dn, dn_w, static_cast<const bf16*>(h_out), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
@@ -477,7 +497,7 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
   if (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
   st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags,
-                  static_cast<uint8_t*>(ws) + partials_bytes(sh.t, M, sh.d) + ticket_bytes(sh.d));
+                  ws);
   if (st != TP_OK) return st;
   st = cuda_status(launch_attn1(static_cast<const bf16*>(qkv_out), M, sh.n_q_heads, sh.n_kv_heads,
                                 sh.head_dim, sh.t, static_cast<bf16*>(o_in), s));
@@ -562,15 +582,15 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   if (M == 0) return TP_OK;
   if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;
   const int t = desc->shape.t, N = (int)desc->rows_per_shard;
-  const uint64_t pb = partials_bytes(t, M, N), need = pb + ticket_bytes(N) + tc_streamk_bytes();
+  const uint64_t pb = partials_bytes(t, M, N), need = sk_bytes() + pb + ticket_bytes(N);
   if (need > kNoallocScratchBytes) return TP_ERR_WORKSPACE;  // beyond the static scratch
   void* scratch = nullptr;
   st = noalloc_scratch(&scratch);
   if (st != TP_OK) return st;
   // the tickets must start at zero; the partials are fully written before they are read
   uint8_t* sc = static_cast<uint8_t*>(scratch);
-  if (cudaMemsetAsync(sc + pb, 0, ticket_bytes(N), S(stream)) != cudaSuccess ||
-      cudaMemsetAsync(sc + need - (size_t)kTcMaxStreamkItems * 4, 0, (size_t)kTcMaxStreamkItems * 4,
+  if (cudaMemsetAsync(sc + sk_bytes(), 0, ticket_bytes(N), S(stream)) != cudaSuccess ||
+      cudaMemsetAsync(sc + tc_streamk_bytes() - (size_t)kTcMaxStreamkItems * 4, 0, (size_t)kTcMaxStreamkItems * 4,
                       S(stream)) != cudaSuccess)
     return TP_ERR_CUDA;
   return run_rowpar(desc, w, static_cast<const bf16*>(a), M, static_cast<const bf16*>(residual),

@@ -53,7 +53,9 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the fast exponential and divide (a few ulp in fp32, far below
+// the bf16 rounding of h); for very negative z the divisor overflows and the result is 0.
+__device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -42,7 +42,7 @@ struct TcCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 1024;  // mbarriers, flags and the stream-K share table
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
 };
 
@@ -119,13 +119,12 @@ struct SegIter {
   }
 };
 
-__device__ __forceinline__ long long share_start(long long total, int G, int c) { return total * c / G; }
-
-// CTA whose stream-K share contains flattened k-block x.
-__device__ __forceinline__ int share_owner(long long total, int G, long long x) {
-  int c = (int)(x * G / total);
-  while (c > 0 && share_start(total, G, c) > x) --c;
-  while (c + 1 < G && share_start(total, G, c + 1) <= x) ++c;
+// Stream-K share boundaries: shares[c] = first flattened k-block of CTA c (shares[G] = total),
+// precomputed once per CTA in shared memory.  CTA owning flattened k-block x:
+__device__ __forceinline__ int share_owner(const uint32_t* shares, uint32_t total, int G, uint32_t x) {
+  int c = (int)((unsigned long long)x * G / total);
+  while (c > 0 && shares[c] > x) --c;
+  while (c + 1 < G && shares[c + 1] <= x) ++c;
   return c;
 }
 
@@ -165,74 +164,145 @@ __device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, in
     for (int j = 0; j < 16; ++j)
       if (mf + j < a.M) a.partials[((size_t)s * a.pM + mf + j) * a.rows + p] = v[j];
   } else {  // TC_ROWPAR_CHAIN: the whole fold is in v already
+    // all residual loads first, then the stores: y may alias the residual, so interleaving
+    // them would cost one memory round trip per token
+    float rv[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      if (mf + j >= a.M) break;
-      const size_t o = (size_t)(mf + j) * a.ldy + p;
-      float val = v[j];
-      if (a.residual) val += __bfloat162float(a.residual[o]);
-      reinterpret_cast<uint16_t*>(a.y)[o] = f2bf(val);
-    }
+    for (int j = 0; j < 16; ++j)
+      rv[j] = (a.residual && mf + j < a.M) ? __bfloat162float(a.residual[(size_t)(mf + j) * a.ldy + p]) : 0.f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (mf + j < a.M) reinterpret_cast<uint16_t*>(a.y)[(size_t)(mf + j) * a.ldy + p] = f2bf(v[j] + rv[j]);
   }
 }
 
-// A CTA that stored one piece of an item: the last of the item's pieces to arrive sums all
-// pieces in k order (piece of CTA c_a first) and runs the item's epilogue.  *done = 1 there.
+// Sync of the 128 epilogue threads on an mbarrier (bounded wait).
+__device__ __forceinline__ bool epi_sync(uint32_t epi_bar, int& phase, volatile int* abort_flag, unsigned code) {
+  mbar_arrive(epi_bar);
+  const bool ok = mbar_wait(epi_bar, phase);
+  phase ^= 1;
+  if (!ok) raise_error(code, abort_flag);
+  return ok;
+}
+
+// Grid-wide barrier of a cooperative (all CTAs co-resident) launch: bar[0] counts arrivals,
+// bar[1] is a generation number that the last arrival bumps.  Bounded wait.
+__device__ bool grid_sync(unsigned* bar, volatile int* abort_flag) {
+  volatile unsigned* gen = bar + 1;
+  const unsigned my = *gen;  // read before arriving: it cannot change until every CTA has arrived
+  __threadfence();
+  if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+    *bar = 0u;
+    __threadfence();
+    atomicAdd(bar + 1, 1u);
+    return true;
+  }
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; *gen == my; ++i) {
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+      raise_error(11, abort_flag);
+      return false;
+    }
+  }
+  __threadfence();
+  return true;
+}
+
+// Emit one output of the item (shard s, row tile rt, token tile tt): `row` is the row inside
+// the 128-row tile, `m` the token.  For SwiGLU `v` is the gate and `u` the up value.
+__device__ __forceinline__ void emit(const TcArgs& a, int s, int rt, int row, int m, float v, float u) {
+  const int p = rt * BM + row;
+  if (a.mode == TC_COLPAR_SWIGLU) {
+    const int f = s * (a.rows / 2) + (p >> 4) * 8 + (p & 7);
+    reinterpret_cast<uint16_t*>(a.out)[(size_t)m * a.ldo + f] = f2bf(silu_f(v) * u);
+  } else if (a.mode == TC_COLPAR_BF16 || a.mode == TC_COLPAR_F32) {
+    const size_t o = (size_t)m * a.ldo + (size_t)s * a.rows + p;
+    if (a.mode == TC_COLPAR_F32)
+      reinterpret_cast<float*>(a.out)[o] = v;
+    else
+      reinterpret_cast<uint16_t*>(a.out)[o] = f2bf(v);
+  } else if (a.mode == TC_ROWPAR_SHARD) {
+    a.partials[((size_t)s * a.pM + m) * a.rows + p] = v;
+  } else {
+    const size_t o = (size_t)m * a.ldy + p;
+    const float r = a.residual ? __bfloat162float(a.residual[o]) : 0.f;
+    reinterpret_cast<uint16_t*>(a.y)[o] = f2bf(v + r);
+  }
+}
+
+// Stream-K fix-up, after the grid barrier.  Every item cut across CTAs is finished by all of
+// its piece owners together: owner j of np sums, in piece (k) order, the pieces' values for
+// its share of the tile's eight 16-row blocks (staged through the idle pipeline smem) and
+// emits those outputs.  One bulk round of loads per piece, spread over the whole grid.
 template <int BN>
-__device__ bool streamk_complete(const TcArgs& a, const Geo& g, const Seg& sg, int s, int p, int m0,
-                                 uint32_t epi_bar, int& phase, volatile int* last_flag,
-                                 volatile int* abort_flag, int* done) {
-  const int G = gridDim.x;
-  const long long total = (long long)g.n_items * g.nkb, istart = (long long)sg.item * g.nkb;
-  const int ca = share_owner(total, G, istart), cb = share_owner(total, G, istart + g.nkb - 1);
-  __threadfence();
-  mbar_arrive(epi_bar);
-  if (!mbar_wait(epi_bar, phase)) {
-    raise_error(9, abort_flag);
-    return false;
-  }
-  phase ^= 1;
-  if (threadIdx.x == 0) {
-    int pieces = 0;  // CTAs between ca and cb with a non-empty share (all of them when G <= total)
-    for (int c = ca; c <= cb; ++c) pieces += share_start(total, G, c + 1) > share_start(total, G, c);
-    const unsigned old = atomicAdd(&a.item_tickets[sg.item], 1u);
-    *last_flag = old == (unsigned)(pieces - 1);
-  }
-  mbar_arrive(epi_bar);
-  if (!mbar_wait(epi_bar, phase)) {
-    raise_error(10, abort_flag);
-    return false;
-  }
-  phase ^= 1;
-  *done = *last_flag;
-  if (!*done) return true;
-  __threadfence();
-  if constexpr (BN <= kTcStreamkMaxBN) {
-    // one L2 round trip per piece: all BN values of this thread's row are requested at once
-    const int r = threadIdx.x;
-    float acc[BN];
+__device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* shares, float* sacc,
+                              uint32_t epi_bar, int& phase, volatile int* abort_flag) {
+  const int G = gridDim.x, tid = threadIdx.x;  // 128 epilogue threads
+  const uint32_t total = shares[G];
+  SegIter segs(true, g);
+  Seg sg;
+  while (segs.next(sg)) {
+    if (sg.kb_lo == 0 && sg.kb_hi == g.nkb) continue;  // whole item: already emitted
+    const uint32_t istart = (uint32_t)sg.item * g.nkb;
+    const int ca = share_owner(shares, total, G, istart), cb = share_owner(shares, total, G, istart + g.nkb - 1);
+    int np = 0, j = -1;
+    for (int c = ca; c <= cb; ++c)
+      if (shares[c + 1] > shares[c]) {
+        if (c == (int)blockIdx.x) j = np;
+        ++np;
+      }
+    const int b0 = j * 8 / np, b1 = (j + 1) * 8 / np;
+    if (b0 == b1) continue;
+    const int r0 = b0 * 16, nr = (b1 - b0) * 16, n4 = nr * BN / 4;
+    // running sums for this thread's float4 slots of the slice ([col][row], rows contiguous)
+    float4 acc[(8 * 16 * BN / 4 + 127) / 128];
+    constexpr int kSlots = (8 * 16 * BN / 4 + 127) / 128;
     bool first = true;
 #pragma unroll 1
     for (int c = ca; c <= cb; ++c) {
-      if (share_start(total, G, c + 1) == share_start(total, G, c)) continue;  // empty share
-      const int slot = share_start(total, G, c) < istart ? 1 : 0;
-      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM + r;
-      float w[BN];
+      if (shares[c + 1] == shares[c]) continue;  // empty share
+      const int slot = shares[c] < istart ? 1 : 0;
+      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM;
 #pragma unroll
-      for (int j = 0; j < BN; ++j) w[j] = __ldcg(src + j * BM);
-#pragma unroll
-      for (int j = 0; j < BN; ++j) acc[j] = first ? w[j] : acc[j] + w[j];
+      for (int k = 0; k < kSlots; ++k) {
+        const int e4 = tid + 128 * k;
+        if (e4 < n4) {
+          const int e = e4 * 4, col = e / nr, row = e % nr;
+          const float4 w = __ldcg(reinterpret_cast<const float4*>(src + (size_t)col * BM + r0 + row));
+          if (first) {
+            acc[k] = w;
+          } else {
+            acc[k].x += w.x; acc[k].y += w.y; acc[k].z += w.z; acc[k].w += w.w;
+          }
+        }
+      }
       first = false;
     }
 #pragma unroll
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      float v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = acc[c0 + j];
-      epilogue_chunk<BN>(a, s, p, m0 + c0, v);
+    for (int k = 0; k < kSlots; ++k) {
+      const int e4 = tid + 128 * k;
+      if (e4 < n4) reinterpret_cast<float4*>(sacc)[e4] = acc[k];
     }
+    if (!epi_sync(epi_bar, phase, abort_flag, 12)) return false;
+    int s, rt, tt;
+    decode_item(a, g, sg.item, s, rt, tt);
+    const int m0 = tt * BN;
+    if (a.mode == TC_COLPAR_SWIGLU) {
+      const int nf = nr / 2;  // 8 features per 16-row block
+      for (int e = tid; e < nf * BN; e += 128) {
+        const int col = e / nf, fl = e % nf, m = m0 + col;
+        if (m >= a.M) continue;
+        const int grow = (fl >> 3) * 16 + (fl & 7);
+        emit(a, s, rt, r0 + grow, m, sacc[col * nr + grow], sacc[col * nr + grow + 8]);
+      }
+    } else {
+      for (int e = tid; e < nr * BN; e += 128) {
+        const int col = e / nr, row = e % nr, m = m0 + col;
+        if (m < a.M) emit(a, s, rt, r0 + row, m, sacc[col * nr + row], 0.f);
+      }
+    }
+    if (!epi_sync(epi_bar, phase, abort_flag, 13)) return false;  // smem reused by the next item
   }
-  if (threadIdx.x == 0) a.item_tickets[sg.item] = 0u;
   return true;
 }
 
@@ -251,12 +321,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 3);
+  uint32_t* shares = tmem_slot + 8;  // [gridDim.x + 1]
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
                  tempty0 = smem_u32(bars + 2 * S + 2), epi_bar = smem_u32(bars + 2 * S + 4),
                  drain_bar = smem_u32(bars + 2 * S + 5);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geo g = make_geo(a, BN);
+
+  // fail fast: after a bounded wait has given up (error word set, cleared by tp_sync), later
+  // launches do nothing instead of each waiting out its own timeouts
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile unsigned*>(&g_tc_error) != 0u;
+  __syncthreads();
+  if (s_skip) return;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
@@ -273,6 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     *last_flag = 0;
     *mma_consumed = 0;
     fence_mbar_init();
+  }
+  if (a.streamk) {  // one share boundary per thread (gridDim.x + 1 <= kThreads)
+    const unsigned long long total = (unsigned long long)g.n_items * g.nkb;
+    for (int c = threadIdx.x; c <= (int)gridDim.x; c += blockDim.x) shares[c] = (uint32_t)(total * c / gridDim.x);
   }
   if (warp == kProducerWarp && lane == 0) {
     tma_prefetch_desc(&tmA);
@@ -294,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The packed weights are not written by the kernel this one may overlap with (under
       // programmatic dependent launch), so the first stages' weight tiles are requested
       // before waiting on it; the activation tiles only after.
+      // weights are streamed once: evict them first so L2 keeps activations and scratch
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
       int pre = 0, pre_xcol[S], pre_row[S];
       {
         SegIter ps(a.streamk != 0, g);
@@ -307,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pre_xcol[pre] = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
             pre_row[pre] = tt * BN;
             mbar_expect_tx(full0 + 8 * pre, C::kABytes);  // stage `pre` is fresh: no empty wait
-            tma_load_3d(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre);
+            tma_load_3d_hint(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre, pol_w);
             ++pre;
           }
         }
@@ -315,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       griddep_wait();
       for (int j = 0; j < pre; ++j) {
         mbar_arrive_expect_tx(full0 + 8 * j, C::kBBytes);
-        tma_load_2d(smem_u32(sB + (size_t)j * C::kBBytes), &tmB, pre_xcol[j], pre_row[j], full0 + 8 * j);
+        tma_load_2d_hint(smem_u32(sB + (size_t)j * C::kBBytes), &tmB, pre_xcol[j], pre_row[j], full0 + 8 * j, pol_x);
       }
       issued = pre;
       SegIter segs(a.streamk != 0, g);
@@ -337,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
           const int xcol = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
           mbar_arrive_expect_tx(full0 + 8 * st, C::kStageBytes);
-          tma_load_3d(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st);
-          tma_load_2d(smem_u32(sB + (size_t)st * C::kBBytes), &tmB, xcol, tt * BN, full0 + 8 * st);
+          tma_load_3d_hint(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st, pol_w);
+          tma_load_2d_hint(smem_u32(sB + (size_t)st * C::kBBytes), &tmB, xcol, tt * BN, full0 + 8 * st, pol_x);
           ++issued;
         }
       }
@@ -406,8 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool whole = sg.kb_lo == 0 && sg.kb_hi == g.nkb;
       float* piece = nullptr;
       if (!whole) {  // this CTA holds one piece of the item: stash it as [col][row]
-        const long long total = (long long)g.n_items * g.nkb, istart = (long long)sg.item * g.nkb;
-        const int slot = share_start(total, gridDim.x, blockIdx.x) < istart ? 1 : 0;
+        const int slot = shares[blockIdx.x] < (uint32_t)sg.item * g.nkb ? 1 : 0;
         piece = a.pieces + ((size_t)blockIdx.x * 2 + slot) * BN * BM;
       }
 #pragma unroll 1
@@ -426,10 +509,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       ++it;
-      if (!whole) {
-        int done = 0;
-        if (!streamk_complete<BN>(a, g, sg, s, p, m0, epi_bar, epi_phase, last_flag, abort_flag, &done)) break;
+    }
+    // stream-K: once every CTA has stored its pieces, the cut items are finished grid-wide
+    if (a.streamk && !*abort_flag) {
+      __threadfence();  // this thread's piece stores are visible device-wide
+      bool ok = epi_sync(epi_bar, epi_phase, abort_flag, 14);
+      if (ok && threadIdx.x == 0) {
+        __threadfence();
+        if (!grid_sync(a.item_tickets, abort_flag)) *last_flag = 1;
       }
+      ok = ok && epi_sync(epi_bar, epi_phase, abort_flag, 15);
+      if constexpr (BN <= kTcStreamkMaxBN)  // wider token tiles never run stream-K
+        if (ok && !*last_flag)
+          streamk_fixup<BN>(a, g, shares, reinterpret_cast<float*>(sA), epi_bar, epi_phase, abort_flag);
     }
   }
 
@@ -521,7 +613,11 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   const int sms = sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid;
   TcArgs b = a;
   // stream-K when the caller gave scratch for it and the tokens fit one decode tile
-  b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items <= kTcMaxStreamkItems;
+  const long long nkb_item = a.mode == TC_ROWPAR_CHAIN ? (long long)a.K / BK * a.t : a.K / BK;
+  // stream-K only when whole items cannot fill the GPU: its cross-CTA fix-up costs more than
+  // the imbalance of item-granular scheduling once every SM has at least one item
+  b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items < sms &&
+              (long long)n_items * nkb_item * kTcMaxGrid < (1ll << 32);  // share table fits 32 bits
   const long long total_kb = (long long)n_items * (a.mode == TC_ROWPAR_CHAIN ? a.K / BK * a.t : a.K / BK);
   const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);
   cudaLaunchConfig_t cfg = {};
@@ -529,11 +625,14 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  // stream-K CTAs meet at a grid barrier: all of them must be resident together
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = b.streamk ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN>, tmA, tmB, b);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -195,3 +195,26 @@ def test_70b_layer_prefill_sampled_rows(dev):
     y_ref, _ = O.mlp(y1b, bits(wg), bits(wu), bits(wd), residual=y1b)
     check_close(bits(y)[rows], y_ref, what="70B MLP block, prefill rows")
     assert not torch.isnan(y).any() and not torch.isnan(y1).any()
+
+
+def test_one_workspace_shared_across_token_counts(dev):
+    """Back-to-back forwards with different M on one workspace (as a serving loop or the bench
+    does): the work-balancing scratch sits at a fixed offset, so every call agrees on it."""
+    d, ffn, t = 4096, 14336, 8
+    sh = tpx.make_shape(d, ffn=ffn, t=t)
+    x0, wg, wu, wd = inputs.mlp_inputs(d, ffn, 64, seed=6, device=dev)
+    gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu)
+    dn_w, dn = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, wd)
+    ws = tpx.new_workspace(sh, 64, dev)
+    wf = [O.as_f64(bits(w)) for w in (wg, wu, wd)]
+    outs = []
+    for M in (32, 64, 32, 1, 64, 17):
+        x = x0[:M].contiguous()
+        y = torch.full_like(x, float("nan"))
+        h = torch.full((M, ffn), float("nan"), dtype=torch.bfloat16, device=dev)
+        tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, x, x, y, h, ws)
+        outs.append((M, x, y))
+    assert tpx.tp_sync(timeout_ms=20000) == tpx.TP_OK
+    for M, x, y in outs:
+        y_ref, _ = O.mlp(bits(x), *wf, residual=bits(x))
+        check_close(bits(y), y_ref, what=f"shared workspace M={M}")
