@@ -251,14 +251,15 @@ def test_tiny_mlp_with_and_without_residual(dev):
     check_close(bits(y0), y0_ref, what="tiny MLP, no residual")
 
 
+@pytest.mark.parametrize("kernel", [0, tpx.TP_F_KERNEL_SKINNY], ids=["default", "skinny"])
 @pytest.mark.parametrize("t", [1, 2, 4, 8])
 @pytest.mark.parametrize("M", [1, 8, 32, 64])
-def test_8b_mlp_decode(dev, t, M):
+def test_8b_mlp_decode(dev, t, M, kernel):
     m = Mlp(4096, 14336, t, M, dev)
-    y, h = m.run()
+    y, h = m.run(flags=kernel)
     y_ref, h_ref = m.oracle()
-    check_close(bits(y), y_ref, what=f"8B MLP t={t} M={M}")
-    y0, _ = m.run(residual=False)
+    check_close(bits(y), y_ref, what=f"8B MLP t={t} M={M} flags={kernel}")
+    y0, _ = m.run(residual=False, flags=kernel)
     y0_ref, _ = m.oracle(residual=False)
     check_close(bits(y0), y0_ref, what=f"8B MLP (no residual) t={t} M={M}")
     check_h(bits(h), h_ref, what="8B h")
