@@ -205,6 +205,12 @@ tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int3
  * (TP_ERR_DEVICE_TIMEOUT) and clears it. */
 tp_status tp_sync(void* stream, int32_t timeout_ms);
 
+/* Diagnostic for the failure path: launches a one-thread kernel whose wait on a barrier that
+ * nothing arrives at gives up after timeout_us (1 .. 1e6) microseconds and records the device
+ * error word, exactly as the library's kernels do when a wait runs out.  The next tp_sync
+ * returns TP_ERR_DEVICE_TIMEOUT and clears it; the context stays usable.  No fault, no trap. */
+tp_status tp_selftest_bounded_wait(int32_t timeout_us, void* stream);
+
 /* Static string for a status code. */
 const char* tp_status_str(tp_status s);
 

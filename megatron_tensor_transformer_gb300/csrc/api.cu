@@ -596,3 +596,8 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   return run_rowpar(desc, w, static_cast<const bf16*>(a), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, scratch, (size_t)need, flags, S(stream));
 }
+
+extern "C" tp_status tp_selftest_bounded_wait(int32_t timeout_us, void* stream) {
+  if (timeout_us < 1 || timeout_us > 1000000) return TP_ERR_INVALID_ARG;
+  return cuda_status(launch_bounded_wait_selftest(timeout_us, S(stream)));
+}

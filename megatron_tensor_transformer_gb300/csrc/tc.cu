@@ -571,6 +571,22 @@ static int sm_count() {
 
 bool tc_supported(int rows, int K, bool fp8) { return !fp8 && rows % BM == 0 && K % BK == 0 && K > 0; }
 
+// Diagnostic: one thread waits on an mbarrier that nothing ever arrives at, with a short
+// limit, and records the error word the way every bounded wait in the library does.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_mbar_init();
+  if (!mbar_wait(b, 0, limit_ns)) atomicExch(&g_tc_error, 100u);
+}
+
+cudaError_t launch_bounded_wait_selftest(int timeout_us, cudaStream_t st) {
+  bounded_wait_selftest_kernel<<<1, 1, 0, st>>>((uint64_t)timeout_us * 1000ull);
+  note_launch();
+  return cudaGetLastError();
+}
+
 unsigned tc_take_device_error() {
   unsigned v = 0, z = 0;
   if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) return 0;

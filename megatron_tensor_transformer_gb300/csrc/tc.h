@@ -49,6 +49,8 @@ bool tc_supported(int rows, int K, bool fp8);
 // pdl: launch as a programmatic dependent of the previous kernel on the stream (the weight
 // tiles stream in while that kernel finishes; activations are read after it completes).
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl);
+// Diagnostic kernel whose single wait is never satisfied and gives up after timeout_us.
+cudaError_t launch_bounded_wait_selftest(int timeout_us, cudaStream_t st);
 // Device error word set by a bounded wait that gave up (0 = none); read and cleared.
 unsigned tc_take_device_error();
 

@@ -22,7 +22,7 @@ TP_F_KERNEL_SKINNY, TP_F_KERNEL_TC, TP_F_SERIAL = 0x10, 0x20, 0x40
 EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspace_bytes",
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
-           "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_sync", "tp_status_str", "tp_launch_count"]
+           "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait", "tp_sync", "tp_status_str", "tp_launch_count"]
 
 
 class TpxError(RuntimeError):
@@ -71,6 +71,7 @@ def lib():
             "tp_noalloc_scratch_capacity": (SZ, []),
             "tp_rmsnorm": (I32, [V, V, ctypes.c_float, I32, I32, V, V]),
             "tp_sync": (I32, [V, I32]),
+            "tp_selftest_bounded_wait": (I32, [I32, V]),
             "tp_status_str": (ctypes.c_char_p, [I32]),
             "tp_launch_count": (ctypes.c_uint64, []),
         }
@@ -202,6 +203,10 @@ def tp_rmsnorm(x, out, eps=1e-5, gain=None, stream=None):
 
 def tp_sync(stream=None, timeout_ms=2000):
     return lib().tp_sync(_stream(stream), timeout_ms)
+
+
+def tp_selftest_bounded_wait(timeout_us, stream=None):
+    _check(lib().tp_selftest_bounded_wait(timeout_us, _stream(stream)), "tp_selftest_bounded_wait")
 
 
 def tp_launch_count():
