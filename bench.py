@@ -123,13 +123,14 @@ def traffic_record():
     kernel source is unchanged since it was taken (else None)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    src = os.path.join(ROOT, "megatron_tensor_transformer_gb300", "csrc", "skinny.cu")
+    src = os.path.join(ROOT, "megatron_tensor_transformer_gb300", "csrc", "tc.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-    return rec if rec.get("skinny_cu_sha256") == h else None
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()
+    return rec if rec.get("tc_cu_sha256") == h else None
 
 
 def oracle_sample(wg, wu, wd, seconds=10.0):
@@ -287,7 +288,7 @@ def run_tpx(args, rank, world, local):
                    "l2": "weights 352 MB per forward > 129 MB L2; no flush"},
         "hbm_gbs_step": step_bytes / (ms_max / K * 1e-3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_max / K * 1e-3) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": "colpar_kernel (gate/up + SwiGLU)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "tc_kernel (gate/up + SwiGLU)", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind + " (hbm_gbs, burst)", "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": None if tr is None else tr.get("bytes_per_launch")},
@@ -302,9 +303,12 @@ def run_tpx(args, rank, world, local):
 
 
 LAYERS = {
-    # name: (d, ffn, n_q, n_kv, hd, t, M)
-    "70b-layer-decode": (8192, 28672, 64, 8, 128, 8, 32),
-    "70b-layer-prefill": (8192, 28672, 64, 8, 128, 8, 4096),
+    # name: (d, ffn, n_q, n_kv, hd, t, M, fp8 weights)
+    "70b-layer-decode": (8192, 28672, 64, 8, 128, 8, 32, False),
+    "70b-layer-prefill": (8192, 28672, 64, 8, 128, 8, 4096, False),
+    "70b-fp8-decode": (8192, 28672, 64, 8, 128, 8, 16, True),
+    "70b-fp8-prefill": (8192, 28672, 64, 8, 128, 8, 8192, True),
+    "405b-layer-decode": (16384, 53248, 128, 8, 128, 8, 16, False),
 }
 
 
@@ -319,12 +323,15 @@ def run_layer(args, rank, world, local):
     import torch
     from megatron_tensor_transformer_gb300 import inputs, tpx
 
-    d, ffn, n_q, n_kv, hd, t, M = LAYERS[args.workload]
+    d, ffn, n_q, n_kv, hd, t, M, fp8 = LAYERS[args.workload]
+    if args.t:
+        t = args.t
     prefill = "prefill" in args.workload
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(device=dev)
-    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
+    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t,
+                        wtype=tpx.TP_FP8_E4M3 if fp8 else tpx.TP_BF16)
     _, wg, wu, wd = inputs.mlp_inputs(d, ffn, 1, seed=0, device=dev)
     gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu, stream=stream)
     dn_w, dn = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, wd, stream=stream)
@@ -370,12 +377,13 @@ def run_layer(args, rank, world, local):
     col_ms = c0.elapsed_time(c1) / K
     params = layer_params(d, ffn, n_q, n_kv, hd)
     flops = 2.0 * params * M
-    wbytes = 2.0 * params
-    col_flops, col_bytes = 2.0 * 2 * d * ffn * M, 2.0 * 2 * d * ffn + 2.0 * M * (d + ffn)
+    wb = 1.0 if fp8 else 2.0          # bytes per weight
+    wbytes = wb * params
+    col_flops, col_bytes = 2.0 * 2 * d * ffn * M, wb * 2 * d * ffn + 2.0 * M * (d + ffn)
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
     out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "steps": K, "warmup": args.warmup,
-           "ms_per_step": ms, "dtype": "bf16", "data": "synthetic",
+           "ms_per_step": ms, "dtype": "e4m3 weights, bf16 math" if fp8 else "bf16", "data": "synthetic",
            "config": {"workload": args.workload, "d": d, "ffn": ffn, "n_q": n_q, "n_kv": n_kv,
                       "head_dim": hd, "t": t, "M": M},
            "gpu_launches": launches, "clocks": clk.summary()}
@@ -441,6 +449,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="8b-mlp-decode", choices=["8b-mlp-decode"] + sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
+    ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny"],
                     help="force the tcgen05 or the mma.sync decode kernel (default: library policy)")
     args = ap.parse_args()

@@ -247,6 +247,8 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     a.mode = mode == COLPAR_SWIGLU ? TC_COLPAR_SWIGLU : (mode == COLPAR_F32 ? TC_COLPAR_F32 : TC_COLPAR_BF16);
     a.w = static_cast<const uint8_t*>(w);
     a.shard_stride = d->shard_stride_bytes;
+    a.fp8 = d->wtype == TP_FP8_E4M3;
+    a.scales_offset = d->scales_offset;
     a.t = t;
     a.rows = rows;
     a.K = K;
@@ -305,6 +307,8 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     TcArgs a{};
     a.w = static_cast<const uint8_t*>(w);
     a.shard_stride = d->shard_stride_bytes;
+    a.fp8 = d->wtype == TP_FP8_E4M3;
+    a.scales_offset = d->scales_offset;
     a.t = t;
     a.rows = N;
     a.K = K;

@@ -33,13 +33,15 @@ using namespace tc;
 static __device__ unsigned g_tc_error;
 
 constexpr int BM = 128, BK = 64;
-constexpr int kThreads = 192, kProducerWarp = 4, kMmaWarp = 5;
+constexpr int kProducerWarp = 4, kMmaWarp = 5;
 
-template <int BN>
+template <int BN, bool FP8 = false>
 struct TcCfg {
-  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kABytes = BM * BK * 2;            // bf16 A tile the MMA reads (SW128)
+  static constexpr int kAqBytes = FP8 ? BM * BK : 0;     // e4m3 A tile as TMA brings it
   static constexpr int kBBytes = BN * BK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStageBytes = kABytes + kBBytes + kAqBytes;
+  static constexpr int kThreadsT = FP8 ? 320 : 192;     // + 4 converter warps for e4m3 weights
   static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kBarBytes = 1024;  // mbarriers, flags and the stream-K share table
@@ -133,9 +135,18 @@ __device__ __forceinline__ void raise_error(unsigned code, volatile int* abort_f
   *abort_flag = 1;
 }
 
+// e4m3 weights: the output channel's fp32 scale (row p of shard s); 1 for bf16 weights.
+__device__ __forceinline__ float row_scale(const TcArgs& a, int s, int p) {
+  return a.fp8 ? reinterpret_cast<const float*>(a.w + (size_t)s * a.shard_stride + a.scales_offset)[p] : 1.f;
+}
+
 // One 16-column chunk of the accumulator for tile row p (of shard s), tokens mf..mf+15.
 template <int BN>
-__device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, int mf, const float (&v)[16]) {
+__device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, int mf, const float (&vin)[16]) {
+  float v[16];
+  const float sc = row_scale(a, s, p);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = vin[j] * sc;
   if (a.mode == TC_COLPAR_SWIGLU) {
     // rows come as [8 gate | 8 up] blocks: the up value of row p sits 8 lanes further on
     float u[16];
@@ -293,12 +304,13 @@ __device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* sha
         const int col = e / nf, fl = e % nf, m = m0 + col;
         if (m >= a.M) continue;
         const int grow = (fl >> 3) * 16 + (fl & 7);
-        emit(a, s, rt, r0 + grow, m, sacc[col * nr + grow], sacc[col * nr + grow + 8]);
+        emit(a, s, rt, r0 + grow, m, sacc[col * nr + grow] * row_scale(a, s, rt * BM + r0 + grow),
+             sacc[col * nr + grow + 8] * row_scale(a, s, rt * BM + r0 + grow + 8));
       }
     } else {
       for (int e = tid; e < nr * BN; e += 128) {
         const int col = e / nr, row = e % nr, m = m0 + col;
-        if (m < a.M) emit(a, s, rt, r0 + row, m, sacc[col * nr + row], 0.f);
+        if (m < a.M) emit(a, s, rt, r0 + row, m, sacc[col * nr + row] * row_scale(a, s, rt * BM + r0 + row), 0.f);
       }
     }
     if (!epi_sync(epi_bar, phase, abort_flag, 13)) return false;  // smem reused by the next item
@@ -306,25 +318,26 @@ __device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* sha
   return true;
 }
 
-template <int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN, bool FP8>
+__global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, FP8>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;                                   // S x [128 rows x 64] bf16, SW128
   uint8_t* sB = smem + (size_t)S * C::kABytes;          // S x [BN rows x 64] bf16, SW128
+  uint8_t* sAq = sB + (size_t)S * C::kBBytes;           // S x [128 rows x 64] e4m3 (FP8 only)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes);
-  // bars: full[S], empty[S], tfull[2], tempty[2], epi, drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  // bars: full[S], empty[S], tfull[2], tempty[2], epi, drain, qfull[S]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 6);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 3);
   uint32_t* shares = tmem_slot + 8;  // [gridDim.x + 1]
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
                  tempty0 = smem_u32(bars + 2 * S + 2), epi_bar = smem_u32(bars + 2 * S + 4),
-                 drain_bar = smem_u32(bars + 2 * S + 5);
+                 drain_bar = smem_u32(bars + 2 * S + 5), qfull0 = smem_u32(bars + 2 * S + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Geo g = make_geo(a, BN);
@@ -338,8 +351,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(full0 + 8 * i, 1);
+      mbar_init(full0 + 8 * i, FP8 ? 1 + 4 : 1);  // + one arrival per converter warp
       mbar_init(empty0 + 8 * i, 1);
+      mbar_init(qfull0 + 8 * i, 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *mma_consumed = 0;
     fence_mbar_init();
   }
-  if (a.streamk) {  // one share boundary per thread (gridDim.x + 1 <= kThreads)
+  if (a.streamk) {  // one share boundary per thread (gridDim.x + 1 <= blockDim.x)
     const unsigned long long total = (unsigned long long)g.n_items * g.nkb;
     for (int c = threadIdx.x; c <= (int)gridDim.x; c += blockDim.x) shares[c] = (uint32_t)(total * c / gridDim.x);
   }
@@ -390,8 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
             pre_xcol[pre] = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
             pre_row[pre] = tt * BN;
-            mbar_expect_tx(full0 + 8 * pre, C::kABytes);  // stage `pre` is fresh: no empty wait
-            tma_load_3d_hint(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre, pol_w);
+            if constexpr (FP8) {  // e4m3 tile to the staging buffer, for the converter warps
+              mbar_arrive_expect_tx(qfull0 + 8 * pre, C::kAqBytes);
+              tma_load_3d_hint(smem_u32(sAq + (size_t)pre * C::kAqBytes), &tmA, kk * BK, rt * BM, ss,
+                               qfull0 + 8 * pre, pol_w);
+            } else {
+              mbar_expect_tx(full0 + 8 * pre, C::kABytes);  // stage `pre` is fresh: no empty wait
+              tma_load_3d_hint(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre,
+                               pol_w);
+            }
             ++pre;
           }
         }
@@ -420,8 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
           const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
           const int xcol = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
-          mbar_arrive_expect_tx(full0 + 8 * st, C::kStageBytes);
-          tma_load_3d_hint(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st, pol_w);
+          if constexpr (FP8) {
+            mbar_arrive_expect_tx(qfull0 + 8 * st, C::kAqBytes);
+            tma_load_3d_hint(smem_u32(sAq + (size_t)st * C::kAqBytes), &tmA, kk * BK, rt * BM, ss, qfull0 + 8 * st,
+                             pol_w);
+            mbar_arrive_expect_tx(full0 + 8 * st, C::kBBytes);
+          } else {
+            mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+            tma_load_3d_hint(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st,
+                             pol_w);
+          }
           tma_load_2d_hint(smem_u32(sB + (size_t)st * C::kBBytes), &tmB, xcol, tt * BN, full0 + 8 * st, pol_x);
           ++issued;
         }
@@ -465,6 +494,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       // wait for every MMA this thread issued before the TMEM can be released
       mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) raise_error(4, abort_flag);
+    }
+  } else if (warp >= 6) {
+    if constexpr (FP8) {
+      // converter warps 6..9: widen each stage's e4m3 weight tile to bf16 in the MMA's
+      // 128-byte-swizzled layout (16-byte chunk j of row r goes to chunk j ^ (r & 7))
+      const int r = (warp - 6) * 32 + lane;
+      int q = 0;
+      SegIter segs(a.streamk != 0, g);
+      Seg sg;
+      bool ok = true;
+      while (ok && !*abort_flag && segs.next(sg)) {
+        for (int kb = sg.kb_lo; kb < sg.kb_hi; ++kb, ++q) {
+          const int st = q % S;
+          if (!__all_sync(0xffffffffu, mbar_wait(qfull0 + 8 * st, (q / S) & 1))) {
+            raise_error(16, abort_flag);
+            ok = false;
+            break;
+          }
+          const uint4* src = reinterpret_cast<const uint4*>(sAq + (size_t)st * C::kAqBytes + r * BK);
+          uint8_t* dst = sA + (size_t)st * C::kABytes + r * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = (c + r) & 3;  // rows start at different 16-byte chunks: fewer bank conflicts
+            const uint4 v = src[cc];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            uint4 lo, hi;
+            lo.x = e4m3x2_to_bf16x2((uint16_t)(w[0] & 0xFFFF));
+            lo.y = e4m3x2_to_bf16x2((uint16_t)(w[0] >> 16));
+            lo.z = e4m3x2_to_bf16x2((uint16_t)(w[1] & 0xFFFF));
+            lo.w = e4m3x2_to_bf16x2((uint16_t)(w[1] >> 16));
+            hi.x = e4m3x2_to_bf16x2((uint16_t)(w[2] & 0xFFFF));
+            hi.y = e4m3x2_to_bf16x2((uint16_t)(w[2] >> 16));
+            hi.z = e4m3x2_to_bf16x2((uint16_t)(w[3] & 0xFFFF));
+            hi.w = e4m3x2_to_bf16x2((uint16_t)(w[3] >> 16));
+            *reinterpret_cast<uint4*>(dst + ((((2 * cc) ^ (r & 7))) * 16)) = lo;
+            *reinterpret_cast<uint4*>(dst + ((((2 * cc + 1) ^ (r & 7))) * 16)) = hi;
+          }
+          // generic-proxy smem writes become visible to the tensor core's async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full0 + 8 * st);
+        }
+      }
     }
   } else {
     // epilogue warps 0..3: every global write comes after the grids this one depends on
@@ -569,7 +641,10 @@ static int sm_count() {
   return n > 0 ? n : 1;
 }
 
-bool tc_supported(int rows, int K, bool fp8) { return !fp8 && rows % BM == 0 && K % BK == 0 && K > 0; }
+bool tc_supported(int rows, int K, bool fp8) {
+  (void)fp8;  // e4m3 weights are widened to bf16 in shared memory
+  return rows % BM == 0 && K % BK == 0 && K > 0;
+}
 
 // Diagnostic: one thread waits on an mbarrier that nothing ever arrives at, with a short
 // limit, and records the error word the way every bounded wait in the library does.
@@ -594,18 +669,21 @@ unsigned tc_take_device_error() {
   return v;
 }
 
-template <int BN>
+template <int BN, bool FP8>
 static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, FP8>;
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.rows, (cuuint64_t)a.t};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.K * 2, (cuuint64_t)a.shard_stride};
+    // bf16: 128-byte-swizzled boxes the MMA reads directly; e4m3: plain 64-byte rows that the
+    // converter warps widen into that layout
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K * (FP8 ? 1 : 2), (cuuint64_t)a.shard_stride};
     const cuuint32_t box[3] = {BK, BM, 1}, es[3] = {1, 1, 1};
-    if (enc(&tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    if (enc(&tmA, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<uint8_t*>(a.w), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            FP8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -620,7 +698,8 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   }
   static bool attr_set = false;  // per instantiation; set before the first launch
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -638,7 +717,7 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(C::kThreadsT);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
@@ -649,19 +728,24 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   attr[1].val.cooperative = b.streamk ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN>, tmA, tmB, b);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, FP8>, tmA, tmB, b);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <bool FP8>
+static cudaError_t tc_bn(const TcArgs& a, cudaStream_t st, bool pdl) {
+  if (a.M <= 16) return tc_go<16, FP8>(a, st, pdl);
+  if (a.M <= 32) return tc_go<32, FP8>(a, st, pdl);
+  if (a.M <= 64) return tc_go<64, FP8>(a, st, pdl);
+  if (a.M <= 128) return tc_go<128, FP8>(a, st, pdl);
+  return tc_go<256, FP8>(a, st, pdl);
+}
+
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl) {
-  if (!tc_supported(a.rows, a.K, false) || a.M <= 0) return cudaErrorInvalidValue;
+  if (!tc_supported(a.rows, a.K, a.fp8 != 0) || a.M <= 0) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x)) & 15) return cudaErrorInvalidValue;
-  if (a.M <= 16) return tc_go<16>(a, st, pdl);
-  if (a.M <= 32) return tc_go<32>(a, st, pdl);
-  if (a.M <= 64) return tc_go<64>(a, st, pdl);
-  if (a.M <= 128) return tc_go<128>(a, st, pdl);
-  return tc_go<256>(a, st, pdl);
+  return a.fp8 ? tc_bn<true>(a, st, pdl) : tc_bn<false>(a, st, pdl);
 }
 
 }  // namespace tpx

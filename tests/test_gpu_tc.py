@@ -218,3 +218,44 @@ def test_one_workspace_shared_across_token_counts(dev):
     for M, x, y in outs:
         y_ref, _ = O.mlp(bits(x), *wf, residual=bits(x))
         check_close(bits(y), y_ref, what=f"shared workspace M={M}")
+
+
+# ---------------------------------------------------------------- FP8 e4m3 weights on tcgen05
+
+
+@pytest.mark.parametrize("t,M", [(8, 16), (2, 1), (4, 130), (8, 300)])
+def test_tc_fp8_mlp(dev, t, M):
+    """e4m3 weights widened to bf16 in shared memory, scales applied per output channel in
+    the epilogue: against the oracle on the dequantised weights (the 3e-2 FP8 bar, and the
+    bf16 bar, which it also meets)."""
+    m = Mlp(2048, 7168, t, M, dev, seed=8, wtype=tpx.TP_FP8_E4M3)
+    y, h = m.run(flags=TC)
+    y_ref, h_ref = m.oracle()
+    check_close(bits(y), y_ref, rel=5e-3, mx=2e-2, what=f"tc fp8 MLP t={t} M={M}")
+    check_h(bits(h), h_ref, what="tc fp8 h")
+    y0, _ = m.run(residual=False, flags=TC)
+    y0_ref, _ = m.oracle(residual=False)
+    check_close(bits(y0), y0_ref, rel=5e-3, mx=2e-2, what=f"tc fp8 MLP no residual t={t} M={M}")
+
+
+def test_tc_fp8_attention_projections(dev):
+    d, n_q, n_kv, hd, t, M = 1024, 8, 4, 128, 4, 48
+    x, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, M, seed=5, device=dev)
+    sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=tpx.TP_FP8_E4M3)
+    q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv)
+    o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo)
+    Q = (n_q + 2 * n_kv) * hd
+    y = torch.full_like(x, float("nan"))
+    qkv = torch.full((M, Q), float("nan"), dtype=torch.bfloat16, device=dev)
+    o_in = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
+    ws = tpx.new_workspace(sh, M, dev)
+    tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y, qkv, o_in, ws, flags=TC)
+    assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
+    deq = []
+    for w in (wqkv, wo):
+        qq, ss = O.quantize_fp8_per_channel(O.as_f64(bits(w)))
+        deq.append(O.dequantize_fp8(qq, ss))
+    y_ref, qkv_ref = O.proj(bits(x), deq[0], deq[1], n_q, n_kv, hd, residual=bits(x))
+    cols = np.concatenate([O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0] for s in range(t)])
+    check_close(bits(qkv), qkv_ref[:, cols], what="tc fp8 qkv")
+    check_close(bits(y), y_ref, what="tc fp8 o_proj")
