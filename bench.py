@@ -404,6 +404,72 @@ def run_layer(args, rank, world, local):
     print(json.dumps(out), flush=True)
 
 
+def run_stack(args, rank, world, local):
+    """Pipeline-stage stack: 10 consecutive 405B-shaped layers (d 16384, ffn 53248, 128 q / 8 kv
+    heads of 128), linear parts + RMSNorm + residual, t=8, bf16, decode M=16, through
+    tp_layer_forward.  63.75 GB of weights, read once per step."""
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+
+    d, ffn, n_q, n_kv, hd, t, M, nl = 16384, 53248, 128, 8, 128, args.t or 8, 16, 10
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
+    layers = []
+    for L in range(nl):
+        _, wg, wu, wd = inputs.mlp_inputs(d, ffn, 1, seed=0, device=dev, layer=L)
+        gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu, stream=stream)
+        dn_w, dn = tpx.tp_partition_weights(sh, tpx.TP_W_DOWN, wd, stream=stream)
+        del wg, wu, wd
+        _, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, 1, seed=0, device=dev, layer=L)
+        q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv, stream=stream)
+        o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo, stream=stream)
+        del wqkv, wo
+        layers.append((q, q_w, o, o_w, gu, gu_w, dn, dn_w))
+        torch.cuda.empty_cache()
+    x0 = inputs.normal_bf16((M, d), 1.0, 0, inputs.STREAM_X, dev)
+    xa, xb = x0.clone(), torch.empty_like(x0)
+    scratch = torch.empty(tpx.tp_layer_scratch_bytes(sh, M), dtype=torch.uint8, device=dev)
+    ws = tpx.new_workspace(sh, M, dev)
+    K = args.steps
+
+    def step():
+        cur, nxt = xa, xb
+        for lay in layers:
+            tpx.tp_layer_forward(*lay, cur, nxt, scratch, ws, stream=stream)
+            cur, nxt = nxt, cur
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            xa.copy_(x0)
+            step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = tpx.tp_launch_count()
+        with Clocks(f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
+            a.record(stream)
+            for _ in range(K):
+                step()
+            b.record(stream)
+            b.synchronize()
+        launches = tpx.tp_launch_count() - n0
+    ms = a.elapsed_time(b) / K
+    wbytes = 2.0 * nl * layer_params(d, ffn, n_q, n_kv, hd)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    print(json.dumps({
+        "metric": METRIC, "workload": "405b-stack-decode", "value": M / (ms * 1e-3), "unit": "tokens/s",
+        "higher_is_better": True, "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "405b-stack-decode", "layers": nl, "d": d, "ffn": ffn, "n_q": n_q, "n_kv": n_kv,
+                   "head_dim": hd, "t": t, "M": M},
+        "weight_gb": wbytes / 1e9, "hbm_gbs_step": wbytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "whole stack", "achieved": wbytes / (ms * 1e-3) / 1e9,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": wbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "gpu_launches": launches, "clocks": clk.summary()}), flush=True)
+
+
 def run_e2e(args, gu, gu_w, dn, dn_w, sh, dev):
     """Through the public C-ABI call tp_mlp_forward with HOST buffers: every step copies each
     batch's x from pinned host memory, runs the block, and copies y back."""
@@ -447,7 +513,8 @@ def main():
     ap.add_argument("--impl", default="tpx", choices=["tpx", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", default="8b-mlp-decode", choices=["8b-mlp-decode"] + sorted(LAYERS),
+    ap.add_argument("--workload", default="8b-mlp-decode",
+                    choices=["8b-mlp-decode", "405b-stack-decode"] + sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny"],
@@ -456,7 +523,9 @@ def main():
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local = dist_setup()
-    if args.workload != "8b-mlp-decode":
+    if args.workload == "405b-stack-decode":
+        run_stack(args, rank, world, local)
+    elif args.workload != "8b-mlp-decode":
         run_layer(args, rank, world, local)
     elif args.impl == "reference":
         run_reference(args, rank, world)

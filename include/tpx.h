@@ -148,6 +148,20 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv /* host */, const void* qkv_
                           const void* residual, int32_t M, void* y, void* qkv_out, void* o_in,
                           void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
+/* One pre-norm Llama layer's linear parts (the pipeline-stage stack is ten of these):
+ *   a = rmsnorm(x);  h1 = x + O(attn(QKV(a)));  b = rmsnorm(h1);  y = h1 + MLP(b)
+ * with RMSNorm eps, gain 1.  The four packed weights must describe one block (same d, t,
+ * dtype; heads for QKV/O, ffn for GATE_UP/DOWN).  x, y: [M, d] bf16 (y may alias x).
+ * scratch: tp_layer_scratch_bytes(shape, M) bytes of device memory for the activations
+ * between the steps (normed inputs, h1, qkv, attention output, h); ws as for the blocks. */
+size_t tp_layer_scratch_bytes(const tp_shape* shape /* host */, int32_t M);
+tp_status tp_layer_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
+                           const tp_packed_desc* o /* host */, const void* o_w,
+                           const tp_packed_desc* gu /* host */, const void* gu_w,
+                           const tp_packed_desc* dn /* host */, const void* dn_w, const void* x,
+                           int32_t M, void* y, float eps, void* scratch, size_t scratch_bytes, void* ws,
+                           size_t ws_bytes, uint32_t flags, void* stream);
+
 /* The "all-reduce" on one GPU: y[m][n] = bf16_rne(((P_0 + P_1) + ... + P_{t-1})[m][n]
  * + float(residual[m][n])), a left fold in shard order (Z = sum_k Z_k, arunshar.com;
  * summation order fixed so results are reproducible).  partials: [t][M][d] fp32;

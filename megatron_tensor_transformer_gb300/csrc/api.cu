@@ -510,6 +510,46 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
                     static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
 }
 
+size_t tp_layer_scratch_bytes(const tp_shape* sh, int32_t M) {
+  if (!sh || M < 0 || sh->d <= 0 || sh->head_dim <= 0 || sh->ffn <= 0) return 0;
+  const uint64_t Q = (uint64_t)(sh->n_q_heads + 2 * sh->n_kv_heads) * sh->head_dim;
+  const uint64_t Mu = (uint64_t)M;
+  // normed input, h1, attention output, normed h1 ([M, d] each), qkv [M, Q], h [M, ffn]
+  return (size_t)(4 * align_up(Mu * sh->d * 2) + align_up(Mu * Q * 2) + align_up(Mu * sh->ffn * 2));
+}
+
+tp_status tp_layer_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp_packed_desc* o,
+                           const void* o_w, const tp_packed_desc* gu, const void* gu_w,
+                           const tp_packed_desc* dn, const void* dn_w, const void* x, int32_t M, void* y,
+                           float eps, void* scratch, size_t scratch_bytes, void* ws, size_t ws_bytes,
+                           uint32_t flags, void* stream) {
+  if (!qkv || !o || !gu || !dn) return TP_ERR_INVALID_ARG;
+  const tp_shape& sa = qkv->shape;
+  const tp_shape& sm = gu->shape;
+  if (sa.d != sm.d || sa.t != sm.t || sa.wtype != sm.wtype) return TP_ERR_LAYOUT_MISMATCH;
+  if (M < 0 || !(eps >= 0.f) || (M > 0 && (!x || !y || !scratch))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  tp_shape both = sa;
+  both.ffn = sm.ffn;
+  if (scratch_bytes < tp_layer_scratch_bytes(&both, M)) return TP_ERR_WORKSPACE;
+  if (!aligned16(scratch)) return TP_ERR_ALIGN;
+  const uint64_t d = sa.d, Q = (uint64_t)(sa.n_q_heads + 2 * sa.n_kv_heads) * sa.head_dim;
+  uint8_t* p = static_cast<uint8_t*>(scratch);
+  void* a = p;  p += align_up((uint64_t)M * d * 2);
+  void* h1 = p; p += align_up((uint64_t)M * d * 2);
+  void* oi = p; p += align_up((uint64_t)M * d * 2);
+  void* b = p;  p += align_up((uint64_t)M * d * 2);
+  void* qk = p; p += align_up((uint64_t)M * Q * 2);
+  void* h = p;
+  tp_status st = tp_rmsnorm(x, nullptr, eps, M, (int32_t)d, a, stream);
+  if (st != TP_OK) return st;
+  st = tp_proj_forward(qkv, qkv_w, o, o_w, a, x, M, h1, qk, oi, ws, ws_bytes, flags, stream);
+  if (st != TP_OK) return st;
+  st = tp_rmsnorm(h1, nullptr, eps, M, (int32_t)d, b, stream);
+  if (st != TP_OK) return st;
+  return tp_mlp_forward(gu, gu_w, dn, dn_w, b, h1, M, y, h, ws, ws_bytes, flags, stream);
+}
+
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,
                      void* stream) {
   if (M < 0 || d <= 0 || !(eps >= 0.f)) return TP_ERR_INVALID_ARG;

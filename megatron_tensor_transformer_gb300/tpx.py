@@ -22,7 +22,8 @@ TP_F_KERNEL_SKINNY, TP_F_KERNEL_TC, TP_F_SERIAL = 0x10, 0x20, 0x40
 EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspace_bytes",
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
-           "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait", "tp_sync", "tp_status_str", "tp_launch_count"]
+           "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
+           "tp_layer_scratch_bytes", "tp_layer_forward", "tp_sync", "tp_status_str", "tp_launch_count"]
 
 
 class TpxError(RuntimeError):
@@ -72,6 +73,9 @@ def lib():
             "tp_rmsnorm": (I32, [V, V, ctypes.c_float, I32, I32, V, V]),
             "tp_sync": (I32, [V, I32]),
             "tp_selftest_bounded_wait": (I32, [I32, V]),
+            "tp_layer_scratch_bytes": (SZ, [P(Shape), I32]),
+            "tp_layer_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V,
+                                       V, I32, V, ctypes.c_float, V, SZ, V, SZ, U32, V]),
             "tp_status_str": (ctypes.c_char_p, [I32]),
             "tp_launch_count": (ctypes.c_uint64, []),
         }
@@ -207,6 +211,18 @@ def tp_sync(stream=None, timeout_ms=2000):
 
 def tp_selftest_bounded_wait(timeout_us, stream=None):
     _check(lib().tp_selftest_bounded_wait(timeout_us, _stream(stream)), "tp_selftest_bounded_wait")
+
+
+def tp_layer_scratch_bytes(shape, M):
+    return lib().tp_layer_scratch_bytes(ctypes.byref(shape), M)
+
+
+def tp_layer_forward(qkv, qkv_w, o, o_w, gu, gu_w, dn, dn_w, x, y, scratch, ws, eps=1e-5, flags=0, stream=None):
+    _check(lib().tp_layer_forward(ctypes.byref(qkv), _ptr(qkv_w), ctypes.byref(o), _ptr(o_w), ctypes.byref(gu),
+                                  _ptr(gu_w), ctypes.byref(dn), _ptr(dn_w), _ptr(x), x.shape[0], _ptr(y), eps,
+                                  _ptr(scratch), scratch.numel(), _ptr(ws), ws.numel(), flags, _stream(stream)),
+           "tp_layer_forward")
+    return y
 
 
 def tp_launch_count():

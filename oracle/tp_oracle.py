@@ -201,11 +201,15 @@ def rmsnorm(x, eps=1e-5, gain=None):
     return a
 
 
-def layer(x, w_qkv, w_o, w_gate, w_up, w_down, n_q, n_kv, hd, eps=1e-5):
+def layer(x, w_qkv, w_o, w_gate, w_up, w_down, n_q, n_kv, hd, eps=1e-5, bf16_between_blocks=False):
     """Pre-norm Llama layer restricted to its linear parts:
-    h = x + O(attn(QKV(rms(x))));  x' = h + MLP(rms(h)).  float64 throughout."""
+    h = x + O(attn(QKV(rms(x))));  x' = h + MLP(rms(h)).  float64 throughout; optionally the
+    attention block's output h is rounded to bf16 (the activation dtype of the configs) before
+    the MLP block reads it."""
     x = as_f64(x)
     hmid, _ = proj(rmsnorm(x, eps), w_qkv, w_o, n_q, n_kv, hd, residual=x)
+    if bf16_between_blocks:
+        hmid = bf16_bits_to_f64(f64_to_bf16_bits(hmid))
     out, _ = mlp(rmsnorm(hmid, eps), w_gate, w_up, w_down, residual=hmid)
     return out, hmid
 

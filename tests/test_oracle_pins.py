@@ -285,3 +285,33 @@ def test_metrics():
     assert O.rel_frobenius(y, y) == 0.0
     assert abs(O.rel_frobenius(y * 1.01, y) - 0.01) < 1e-12
     assert abs(O.max_err_over_rms(y + np.array([[0.0, 0.5]]), y) - 0.5 / math.sqrt(12.5)) < 1e-12
+
+
+# ---------------------------------------------------------------- the pre-norm layer
+
+
+def _layer_weights(rng, d=32, ffn=64, n_q=4, n_kv=2, hd=8):
+    q = (n_q + 2 * n_kv) * hd
+    return (rng.normal(size=(d, q)) * 0.2, rng.normal(size=(n_q * hd, d)) * 0.2, rng.normal(size=(d, ffn)) * 0.2,
+            rng.normal(size=(d, ffn)) * 0.2, rng.normal(size=(ffn, d)) * 0.2)
+
+
+def test_layer_reduces_to_its_blocks():
+    rng = np.random.default_rng(12)
+    d = 32
+    x = O.bf16_bits_to_f64(O.f64_to_bf16_bits(rng.normal(size=(3, d))))   # bf16-valued input
+    wqkv, wo, wg, wu, wd = _layer_weights(rng)
+    # attention output projection zero: h = x exactly, layer = x + MLP(rms(x))
+    y, h = O.layer(x, wqkv, np.zeros_like(wo), wg, wu, wd, 4, 2, 8)
+    assert np.array_equal(h, x)
+    m, _ = O.mlp(O.rmsnorm(x), wg, wu, wd, residual=x)
+    assert np.allclose(y, m, rtol=1e-13, atol=1e-13)
+    # MLP down projection zero: the layer is the (bf16-stored) attention block
+    y, h = O.layer(x, wqkv, wo, wg, wu, np.zeros_like(wd), 4, 2, 8, bf16_between_blocks=True)
+    p, _ = O.proj(O.rmsnorm(x), wqkv, wo, 4, 2, 8, residual=x)
+    assert np.array_equal(y, O.bf16_bits_to_f64(O.f64_to_bf16_bits(p)))
+    # by default the layer is the two blocks composed in float64
+    y, _ = O.layer(x, wqkv, wo, wg, wu, wd, 4, 2, 8)
+    m, _ = O.mlp(O.rmsnorm(p), wg, wu, wd, residual=p)
+    assert np.allclose(y, m, rtol=1e-13, atol=1e-13)
+
