@@ -225,6 +225,10 @@ tp_status tp_sync(void* stream, int32_t timeout_ms);
  * returns TP_ERR_DEVICE_TIMEOUT and clears it; the context stays usable.  No fault, no trap. */
 tp_status tp_selftest_bounded_wait(int32_t timeout_us, void* stream);
 
+/* Diagnostic: decode n e4m3 codes (bytes, n % 4 == 0) to bf16 with the exact routine the FP8
+ * weight path widens weight tiles with, so a test can compare every code with its value. */
+tp_status tp_selftest_e4m3_decode(const void* codes, void* out, int32_t n, void* stream);
+
 /* Static string for a status code. */
 const char* tp_status_str(tp_status s);
 

@@ -645,3 +645,9 @@ extern "C" tp_status tp_selftest_bounded_wait(int32_t timeout_us, void* stream) 
   if (timeout_us < 1 || timeout_us > 1000000) return TP_ERR_INVALID_ARG;
   return cuda_status(launch_bounded_wait_selftest(timeout_us, S(stream)));
 }
+
+extern "C" tp_status tp_selftest_e4m3_decode(const void* codes, void* out, int32_t n, void* stream) {
+  if (!codes || !out || n <= 0 || n % 4) return TP_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(out)) return TP_ERR_ALIGN;
+  return cuda_status(launch_e4m3_decode(codes, out, n, S(stream)));
+}

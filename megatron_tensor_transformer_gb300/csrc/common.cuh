@@ -53,6 +53,24 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint16_t v) {
   return *reinterpret_cast<uint32_t*>(&b);
 }
 
+// Four e4m3 codes (byte i of w = element i) -> four bf16 values (.x = elements 0,1; .y =
+// elements 2,3), exactly, with integer ops and one bf16x2 multiply per pair (no conversion
+// instructions).  Each code's sign goes to bit 15 of a 16-bit half and its 7 exponent+mantissa
+// bits to bits 10..4: read as bf16 that is the code's value times 2^-120 (a normal code's
+// exponent field reads e against bias 127 instead of 7; a subnormal code and zero line their
+// 3 mantissa bits up under a zero exponent field in both formats).  Multiplying by 2^120 is
+// exact.  Even elements are placed with left shifts, odd ones with right shifts; a byte
+// permute puts the pairs back in order.
+__device__ __forceinline__ uint2 e4m3x4_to_bf16x4(uint32_t w) {
+  const uint32_t k = 0x7B807B80u;  // bf16x2 (2^120, 2^120)
+  const uint32_t ev = ((w << 4) & 0x07F007F0u) | ((w << 8) & 0x80008000u);  // elements 0, 2
+  const uint32_t od = ((w >> 4) & 0x07F007F0u) | (w & 0x80008000u);         // elements 1, 3
+  uint32_t e2, o2;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(e2) : "r"(ev), "r"(k));
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(o2) : "r"(od), "r"(k));
+  return make_uint2(__byte_perm(e2, o2, 0x5410), __byte_perm(e2, o2, 0x7632));
+}
+
 // silu(z) = z / (1 + e^-z) with the fast exponential and divide (a few ulp in fp32, far below
 // the bf16 rounding of h); for very negative z the divisor overflows and the result is 0.
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }

@@ -41,7 +41,8 @@ struct TcCfg {
   static constexpr int kAqBytes = FP8 ? BM * BK : 0;     // e4m3 A tile as TMA brings it
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes + kAqBytes;
-  static constexpr int kThreadsT = FP8 ? 320 : 192;     // + 4 converter warps for e4m3 weights
+  static constexpr int kConvWarps = FP8 ? 8 : 0;        // converter warps for e4m3 weights
+  static constexpr int kThreadsT = 192 + 32 * kConvWarps;
   static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kBarBytes = 1024;  // mbarriers, flags and the stream-K share table
@@ -265,34 +266,39 @@ __device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* sha
     const int b0 = j * 8 / np, b1 = (j + 1) * 8 / np;
     if (b0 == b1) continue;
     const int r0 = b0 * 16, nr = (b1 - b0) * 16, n4 = nr * BN / 4;
-    // running sums for this thread's float4 slots of the slice ([col][row], rows contiguous)
-    float4 acc[(8 * 16 * BN / 4 + 127) / 128];
-    constexpr int kSlots = (8 * 16 * BN / 4 + 127) / 128;
-    bool first = true;
+    // running sums for this thread's float4 slots of the slice ([col][row], rows contiguous),
+    // at most 8 slots (32 registers) per pass over the pieces
+    constexpr int kSlotsAll = (8 * 16 * BN / 4 + 127) / 128;
+    constexpr int kSlots = kSlotsAll > 8 ? 8 : kSlotsAll;
 #pragma unroll 1
-    for (int c = ca; c <= cb; ++c) {
-      if (shares[c + 1] == shares[c]) continue;  // empty share
-      const int slot = shares[c] < istart ? 1 : 0;
-      const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM;
+    for (int k0 = 0; k0 < kSlotsAll; k0 += kSlots) {
+      float4 acc[kSlots];
+      bool first = true;
+#pragma unroll 1
+      for (int c = ca; c <= cb; ++c) {
+        if (shares[c + 1] == shares[c]) continue;  // empty share
+        const int slot = shares[c] < istart ? 1 : 0;
+        const float* src = a.pieces + ((size_t)c * 2 + slot) * BN * BM;
 #pragma unroll
-      for (int k = 0; k < kSlots; ++k) {
-        const int e4 = tid + 128 * k;
-        if (e4 < n4) {
-          const int e = e4 * 4, col = e / nr, row = e % nr;
-          const float4 w = __ldcg(reinterpret_cast<const float4*>(src + (size_t)col * BM + r0 + row));
-          if (first) {
-            acc[k] = w;
-          } else {
-            acc[k].x += w.x; acc[k].y += w.y; acc[k].z += w.z; acc[k].w += w.w;
+        for (int k = 0; k < kSlots; ++k) {
+          const int e4 = tid + 128 * (k0 + k);
+          if (e4 < n4) {
+            const int e = e4 * 4, col = e / nr, row = e % nr;
+            const float4 w = __ldcg(reinterpret_cast<const float4*>(src + (size_t)col * BM + r0 + row));
+            if (first) {
+              acc[k] = w;
+            } else {
+              acc[k].x += w.x; acc[k].y += w.y; acc[k].z += w.z; acc[k].w += w.w;
+            }
           }
         }
+        first = false;
       }
-      first = false;
-    }
 #pragma unroll
-    for (int k = 0; k < kSlots; ++k) {
-      const int e4 = tid + 128 * k;
-      if (e4 < n4) reinterpret_cast<float4*>(sacc)[e4] = acc[k];
+      for (int k = 0; k < kSlots; ++k) {
+        const int e4 = tid + 128 * (k0 + k);
+        if (e4 < n4) reinterpret_cast<float4*>(sacc)[e4] = acc[k];
+      }
     }
     if (!epi_sync(epi_bar, phase, abort_flag, 12)) return false;
     int s, rt, tt;
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(full0 + 8 * i, FP8 ? 1 + 4 : 1);  // + one arrival per converter warp
+      mbar_init(full0 + 8 * i, 1 + C::kConvWarps);  // + one arrival per converter warp
       mbar_init(empty0 + 8 * i, 1);
       mbar_init(qfull0 + 8 * i, 1);
     }
@@ -497,9 +503,15 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
     }
   } else if (warp >= 6) {
     if constexpr (FP8) {
-      // converter warps 6..9: widen each stage's e4m3 weight tile to bf16 in the MMA's
-      // 128-byte-swizzled layout (16-byte chunk j of row r goes to chunk j ^ (r & 7))
-      const int r = (warp - 6) * 32 + lane;
+      // converter warps: widen each stage's e4m3 weight tile ([128 rows][64 bytes]) to bf16 in
+      // the MMA's 128-byte-swizzled layout (16-byte chunk j of row r goes to chunk j ^ (r & 7)).
+      // A unit is one 16-byte e4m3 chunk (row, cc) -> bf16 chunks 2cc, 2cc+1.  Each group of 8
+      // lanes takes two adjacent rows x 4 chunks: its 16-byte reads cover 128 distinct bytes
+      // mod 128 and so do its writes (rows r, r+1 swizzle by an even and an odd mask), so
+      // neither side has bank conflicts.
+      constexpr int kRowsPerWarp = BM / C::kConvWarps;
+      const int cw = warp - 6, p8 = lane >> 3, q8 = lane & 7;
+      const int cc = q8 & 3;
       int q = 0;
       SegIter segs(a.streamk != 0, g);
       Seg sg;
@@ -512,24 +524,22 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
             ok = false;
             break;
           }
-          const uint4* src = reinterpret_cast<const uint4*>(sAq + (size_t)st * C::kAqBytes + r * BK);
-          uint8_t* dst = sA + (size_t)st * C::kABytes + r * 128;
+          const uint8_t* srcs = sAq + (size_t)st * C::kAqBytes;
+          uint8_t* dsts = sA + (size_t)st * C::kABytes;
+          uint4 v[kRowsPerWarp / 8];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int cc = (c + r) & 3;  // rows start at different 16-byte chunks: fewer bank conflicts
-            const uint4 v = src[cc];
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint4 lo, hi;
-            lo.x = e4m3x2_to_bf16x2((uint16_t)(w[0] & 0xFFFF));
-            lo.y = e4m3x2_to_bf16x2((uint16_t)(w[0] >> 16));
-            lo.z = e4m3x2_to_bf16x2((uint16_t)(w[1] & 0xFFFF));
-            lo.w = e4m3x2_to_bf16x2((uint16_t)(w[1] >> 16));
-            hi.x = e4m3x2_to_bf16x2((uint16_t)(w[2] & 0xFFFF));
-            hi.y = e4m3x2_to_bf16x2((uint16_t)(w[2] >> 16));
-            hi.z = e4m3x2_to_bf16x2((uint16_t)(w[3] & 0xFFFF));
-            hi.w = e4m3x2_to_bf16x2((uint16_t)(w[3] >> 16));
-            *reinterpret_cast<uint4*>(dst + ((((2 * cc) ^ (r & 7))) * 16)) = lo;
-            *reinterpret_cast<uint4*>(dst + ((((2 * cc + 1) ^ (r & 7))) * 16)) = hi;
+          for (int it = 0; it < kRowsPerWarp / 8; ++it) {
+            const int r = kRowsPerWarp * cw + 2 * (4 * it + p8) + (q8 >> 2);
+            v[it] = *reinterpret_cast<const uint4*>(srcs + r * BK + cc * 16);
+          }
+#pragma unroll
+          for (int it = 0; it < kRowsPerWarp / 8; ++it) {
+            const int r = kRowsPerWarp * cw + 2 * (4 * it + p8) + (q8 >> 2);
+            const uint2 c0 = e4m3x4_to_bf16x4(v[it].x), c1 = e4m3x4_to_bf16x4(v[it].y);
+            const uint2 c2 = e4m3x4_to_bf16x4(v[it].z), c3 = e4m3x4_to_bf16x4(v[it].w);
+            uint8_t* dst = dsts + r * 128;
+            *reinterpret_cast<uint4*>(dst + (((2 * cc) ^ (r & 7)) * 16)) = make_uint4(c0.x, c0.y, c1.x, c1.y);
+            *reinterpret_cast<uint4*>(dst + (((2 * cc + 1) ^ (r & 7)) * 16)) = make_uint4(c2.x, c2.y, c3.x, c3.y);
           }
           // generic-proxy smem writes become visible to the tensor core's async proxy
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -658,6 +668,19 @@ __global__ void bounded_wait_selftest_kernel(uint64_t limit_ns) {
 
 cudaError_t launch_bounded_wait_selftest(int timeout_us, cudaStream_t st) {
   bounded_wait_selftest_kernel<<<1, 1, 0, st>>>((uint64_t)timeout_us * 1000ull);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// Diagnostic: decode n e4m3 codes with the converter's routine (n a multiple of 4).
+__global__ void e4m3_decode_kernel(const uint32_t* codes, uint2* out, int n4) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n4) out[i] = e4m3x4_to_bf16x4(codes[i]);
+}
+
+cudaError_t launch_e4m3_decode(const void* codes, void* out, int n, cudaStream_t st) {
+  const int n4 = n / 4;
+  e4m3_decode_kernel<<<(n4 + 255) / 256, 256, 0, st>>>(static_cast<const uint32_t*>(codes), static_cast<uint2*>(out), n4);
   note_launch();
   return cudaGetLastError();
 }

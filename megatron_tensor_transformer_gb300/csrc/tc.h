@@ -53,6 +53,8 @@ bool tc_supported(int rows, int K, bool fp8);
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl);
 // Diagnostic kernel whose single wait is never satisfied and gives up after timeout_us.
 cudaError_t launch_bounded_wait_selftest(int timeout_us, cudaStream_t st);
+// Diagnostic: the FP8 converter's e4m3 -> bf16 routine over n codes (n % 4 == 0).
+cudaError_t launch_e4m3_decode(const void* codes, void* out, int n, cudaStream_t st);
 // Device error word set by a bounded wait that gave up (0 = none); read and cleared.
 unsigned tc_take_device_error();
 

@@ -23,7 +23,7 @@ EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspa
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
            "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
-           "tp_layer_scratch_bytes", "tp_layer_forward", "tp_sync", "tp_status_str", "tp_launch_count"]
+           "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count"]
 
 
 class TpxError(RuntimeError):
@@ -74,6 +74,7 @@ def lib():
             "tp_sync": (I32, [V, I32]),
             "tp_selftest_bounded_wait": (I32, [I32, V]),
             "tp_layer_scratch_bytes": (SZ, [P(Shape), I32]),
+            "tp_selftest_e4m3_decode": (I32, [V, V, I32, V]),
             "tp_layer_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V,
                                        V, I32, V, ctypes.c_float, V, SZ, V, SZ, U32, V]),
             "tp_status_str": (ctypes.c_char_p, [I32]),
@@ -223,6 +224,12 @@ def tp_layer_forward(qkv, qkv_w, o, o_w, gu, gu_w, dn, dn_w, x, y, scratch, ws, 
                                   _ptr(scratch), scratch.numel(), _ptr(ws), ws.numel(), flags, _stream(stream)),
            "tp_layer_forward")
     return y
+
+
+def tp_selftest_e4m3_decode(codes, out, stream=None):
+    _check(lib().tp_selftest_e4m3_decode(_ptr(codes), _ptr(out), codes.numel(), _stream(stream)),
+           "tp_selftest_e4m3_decode")
+    return out
 
 
 def tp_launch_count():

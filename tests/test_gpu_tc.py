@@ -259,3 +259,17 @@ def test_tc_fp8_attention_projections(dev):
     cols = np.concatenate([O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0] for s in range(t)])
     check_close(bits(qkv), qkv_ref[:, cols], what="tc fp8 qkv")
     check_close(bits(y), y_ref, what="tc fp8 o_proj")
+
+
+def test_fp8_widening_is_exact_for_every_code(dev):
+    """The converter's integer-plus-multiply e4m3 -> bf16 widening against the oracle's decode
+    of every one of the 256 codes (NaN codes aside: quantised weights are finite)."""
+    codes = torch.arange(256, dtype=torch.uint8, device=dev)
+    out = torch.empty(256, dtype=torch.bfloat16, device=dev)
+    tpx.tp_selftest_e4m3_decode(codes, out)
+    torch.cuda.synchronize()
+    want = O.e4m3_bits_to_f64(np.arange(256, dtype=np.uint8))
+    got = O.as_f64(bits(out))
+    finite = ~np.isnan(want)
+    assert np.array_equal(got[finite], want[finite])
+    assert np.array_equal(np.signbit(got[finite]), np.signbit(want[finite]))   # -0 stays -0
