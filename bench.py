@@ -1,7 +1,8 @@
 """Benchmark: Llama-3-8B-shaped tensor-parallel MLP layer, decode, t=8 logical shards on one GPU.
 
 One step = one SwiGLU MLP forward (column-parallel gate/up + SwiGLU, row-parallel down +
-fixed-order shard fold + residual) for each decode batch M in {1, 8, 32, 64}: 105 tokens.
+fixed-order shard fold + residual) through tp_mlp_forward for each decode batch M in
+{1, 8, 32, 64}: 105 tokens.  By default each forward is one fused block launch.
 Weights are 352 MB (> 129 MB L2), read once per forward, so no L2 flush is needed between
 forwards.  Prints one JSON line (see the fields below).
 
@@ -40,12 +41,8 @@ def weight_bytes():
     return 3 * D * FFN * 2
 
 
-def colpar_bytes(M):     # gate/up weights + x in + h out
-    return 2 * D * FFN * 2 + M * D * 2 + M * FFN * 2
-
-
-def rowpar_bytes(M):     # down weights + h in + residual in + y out
-    return FFN * D * 2 + M * FFN * 2 + 2 * M * D * 2
+def block_bytes(M):      # all three weights + x in + residual in + y out (h stays on chip/L2)
+    return 3 * D * FFN * 2 + 3 * M * D * 2
 
 
 class Clocks:
@@ -119,18 +116,20 @@ def max_over_ranks(v, world, dev):
 
 
 def traffic_record():
-    """Per-launch DRAM traffic of the gate/up kernel from the committed ncu summary, if the
-    kernel source is unchanged since it was taken (else None)."""
+    """Per-launch DRAM traffic of the dominant kernel from the committed ncu summary, if the
+    kernel's source file is unchanged since the counters were taken (else None)."""
     import hashlib
     p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
-    src = os.path.join(ROOT, "megatron_tensor_transformer_gb300", "csrc", "tc.cu")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         rec = json.load(f)
+    src = os.path.join(ROOT, "megatron_tensor_transformer_gb300", "csrc", rec.get("source", ""))
+    if not os.path.isfile(src):
+        return None
     with open(src, "rb") as f:
         h = hashlib.sha256(f.read()).hexdigest()
-    return rec if rec.get("tc_cu_sha256") == h else None
+    return rec if rec.get("sha256") == h else None
 
 
 def oracle_sample(wg, wu, wd, seconds=10.0):
@@ -223,20 +222,18 @@ def run_tpx(args, rank, world, local):
     hs = {M: torch.empty((M, FFN), dtype=torch.bfloat16, device=dev) for M in MS}
     ys = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
     ws = tpx.new_workspace(sh, max(MS), dev)
-    kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY}[args.kernel]
+    kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY,
+          "split": tpx.TP_F_SPLIT_BLOCK}[args.kernel]
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in MS] for _ in range(K)]
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in MS] for _ in range(K)]
 
     def step(i=None):
         for j, M in enumerate(MS):
             if i is not None:
                 ev[i][j][0].record(stream)
-            tpx.tp_colpar_forward(gu, gu_w, xs[M], hs[M], flags=kf, stream=stream, ws=ws)
+            tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, xs[M], xs[M], ys[M], hs[M], ws, flags=kf, stream=stream)
             if i is not None:
                 ev[i][j][1].record(stream)
-            tpx.tp_rowpar_forward(dn, dn_w, hs[M], xs[M], ys[M], ws, flags=kf, stream=stream)
-            if i is not None:
-                ev[i][j][2].record(stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -256,39 +253,38 @@ def run_tpx(args, rank, world, local):
         launches = tpx.tp_launch_count() - n0
         torch.cuda.synchronize()
         barrier(world)
-        # second pass, same work, with an event around every kernel: per-kernel durations
+        # second pass, same work, with an event around every forward: per-forward durations
         for i in range(K):
             step(i)
         torch.cuda.synchronize()
     ms = t_start.elapsed_time(t_end)
     ms_max = max_over_ranks(ms, world, dev)
     per_M = {}
-    col_t = col_b = 0.0
+    blk_t = blk_b = 0.0
     for j, M in enumerate(MS):
         c = sum(ev[i][j][0].elapsed_time(ev[i][j][1]) for i in range(K)) / K
-        r = sum(ev[i][j][1].elapsed_time(ev[i][j][2]) for i in range(K)) / K
-        col_t += c
-        col_b += colpar_bytes(M)
-        per_M[str(M)] = {"tokens_per_s": M / ((c + r) * 1e-3), "colpar_us": 1e3 * c, "rowpar_us": 1e3 * r,
-                         "colpar_gbs": colpar_bytes(M) / (c * 1e-3) / 1e9,
-                         "rowpar_gbs": rowpar_bytes(M) / (r * 1e-3) / 1e9,
-                         "layer_gbs": (colpar_bytes(M) + rowpar_bytes(M)) / ((c + r) * 1e-3) / 1e9}
+        blk_t += c
+        blk_b += block_bytes(M)
+        per_M[str(M)] = {"tokens_per_s": M / (c * 1e-3), "block_us": 1e3 * c,
+                         "block_gbs": block_bytes(M) / (c * 1e-3) / 1e9}
     peak, peak_kind = peaks()
-    achieved = col_b / (col_t * 1e-3) / 1e9
+    achieved = blk_b / (blk_t * 1e-3) / 1e9
     tr = traffic_record()
     e2e = run_e2e(args, gu, gu_w, dn, dn_w, sh, dev)
     tokens = sum(MS) * K * world
-    step_bytes = sum(colpar_bytes(M) + rowpar_bytes(M) for M in MS)
+    step_bytes = sum(block_bytes(M) for M in MS)
+    kname = {"auto": "fused_kernel (whole MLP block, one launch per forward)", "tc": "fused_kernel",
+             "skinny": "colpar/rowpar mma.sync kernels + fold", "split": "tc_kernel x2 + fold"}[args.kernel]
     out = {
         "metric": METRIC, "value": tokens / (ms_max * 1e-3), "unit": "tokens/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": ms_max / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "d": D, "ffn": FFN, "t": T, "M": list(MS),
                    "tokens_per_step": sum(MS), "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "weights 352 MB per forward > 129 MB L2; no flush"},
+                   "l2": "weights 352 MB per forward > 129 MB L2; no flush", "kernel": args.kernel},
         "hbm_gbs_step": step_bytes / (ms_max / K * 1e-3) / 1e9,
         "hbm_frac_step": step_bytes / (ms_max / K * 1e-3) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": "tc_kernel (gate/up + SwiGLU)", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": kname, "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind + " (hbm_gbs, burst)", "unit": "GB/s",
                      "frac": achieved / peak,
                      "traffic": None if tr is None else tr.get("bytes_per_launch")},
@@ -366,11 +362,15 @@ def run_layer(args, rank, world, local):
             b.record(stream)
             b.synchronize()
         launches = tpx.tp_launch_count() - n0
-        # dominant kernel alone: the MLP's column-parallel gate/up + SwiGLU
+        # dominant kernel alone: decode, the MLP block (one fused launch for bf16 weights);
+        # prefill, the MLP's column-parallel gate/up + SwiGLU
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         c0.record(stream)
         for _ in range(K):
-            tpx.tp_colpar_forward(gu, gu_w, y1, h, stream=stream, ws=ws)
+            if prefill:
+                tpx.tp_colpar_forward(gu, gu_w, y1, h, stream=stream, ws=ws)
+            else:
+                tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, stream=stream)
         c1.record(stream)
         c1.synchronize()
     ms = a.elapsed_time(b) / K
@@ -379,7 +379,8 @@ def run_layer(args, rank, world, local):
     flops = 2.0 * params * M
     wb = 1.0 if fp8 else 2.0          # bytes per weight
     wbytes = wb * params
-    col_flops, col_bytes = 2.0 * 2 * d * ffn * M, wb * 2 * d * ffn + 2.0 * M * (d + ffn)
+    col_flops = 2.0 * 2 * d * ffn * M
+    col_bytes = wb * 3 * d * ffn + 2.0 * 3 * M * d     # decode: the whole MLP block
     with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
         pk = json.load(f)
     out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "steps": K, "warmup": args.warmup,
@@ -397,7 +398,7 @@ def run_layer(args, rank, world, local):
     else:
         out.update({"value": M / (ms * 1e-3), "unit": "tokens/s", "higher_is_better": True,
                     "hbm_gbs_step": wbytes / (ms * 1e-3) / 1e9,
-                    "roofline": {"bound": "hbm", "kernel": "tc_kernel (gate/up + SwiGLU)",
+                    "roofline": {"bound": "hbm", "kernel": "MLP block (tp_mlp_forward)",
                                  "achieved": col_bytes / (col_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"],
                                  "unit": "GB/s", "frac": col_bytes / (col_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
                                  "layer_frac": wbytes / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}})
@@ -517,8 +518,9 @@ def main():
                     choices=["8b-mlp-decode", "405b-stack-decode"] + sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny"],
-                    help="force the tcgen05 or the mma.sync decode kernel (default: library policy)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny", "split"],
+                    help="force the tcgen05 or the mma.sync decode kernels, or separate launches for the "
+                         "two halves of a block (default: library policy, one fused launch per block)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -105,6 +105,12 @@ typedef struct {
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernel (bf16 weights, rows % 128, K % 64);
                                      default: tcgen05 where supported, else mma.sync */
+#define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
+                                     launches.  By default a decode block (M <= 64, bf16 weights, 128-row
+                                     and 64-k tiles) runs as ONE persistent launch: the column-parallel
+                                     items, then the row-parallel items, each of which waits only for its
+                                     own shard's first half; the last shard of each 128-row output tile
+                                     folds the t partials in shard order (same bits as the split path) */
 
 /* Size in bytes of the packed buffer for (shape, kind); 0 if the shape is invalid. */
 size_t tp_packed_bytes(const tp_shape* shape /* host */, int32_t kind);
@@ -124,7 +130,8 @@ tp_status tp_partition_weights(const tp_shape* shape /* host */, int32_t kind, c
                                tp_packed_desc* desc_out /* host */, void* stream);
 
 /* Workspace bytes the forward calls need for M tokens (shard partials and tickets).
- * The workspace must be zero-filled once before first use; calls leave it reusable. */
+ * The workspace must be zero-filled once before first use; calls leave it reusable.  After a
+ * call has ended in TP_ERR_DEVICE_TIMEOUT (reported by tp_sync), zero-fill it again. */
 size_t tp_workspace_bytes(const tp_shape* shape /* host */, int32_t M, uint32_t flags);
 
 /* SwiGLU MLP block: h = silu(x Wg) * (x Wu) column-parallel per shard, then

@@ -7,6 +7,7 @@
 #include <thread>
 
 #include "common.cuh"
+#include "fused.h"
 #include "pack.h"
 #include "skinny.h"
 #include "small.h"
@@ -202,7 +203,7 @@ using bf16 = __nv_bfloat16;
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 0;  // tcgen05 wherever the geometry allows: with PDL it wins the whole step
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
-constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL;
+constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
@@ -385,6 +386,50 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   return TP_OK;
 }
 
+// Sync words of the fused block kernel: inside the stream-K ticket area, past the grid-barrier
+// words that the stream-K path uses (offsets independent of M, zero between calls).
+unsigned* fused_sync(void* ws) {
+  return reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + tc_streamk_bytes() -
+                                     (size_t)kTcMaxStreamkItems * 4) + 64;
+}
+
+// One persistent launch for the whole block (decode token counts, bf16 weights), unless the
+// flags ask for separate launches or for the mma.sync kernels.
+bool pick_fused(uint32_t flags, const tp_packed_desc* d1, const tp_packed_desc* d2, int M) {
+  if (flags & (TP_F_UNFUSED_REDUCE | TP_F_KERNEL_SKINNY | TP_F_SPLIT_BLOCK)) return false;
+  if (d1->wtype != TP_BF16) return false;
+  return fused_supported((int)d1->rows_per_shard, d1->shape.d, (int)d2->k_per_shard, M, d1->shape.t);
+}
+
+tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp_packed_desc* d2, const void* w2,
+                    const bf16* x, const bf16* res, int M, bf16* y, bf16* mid, bf16* mid2, void* ws,
+                    uint32_t flags, cudaStream_t st) {
+  FusedArgs a{};
+  a.kind = kind;
+  a.t = d1->shape.t;
+  a.M = M;
+  a.d = d1->shape.d;
+  a.w1 = static_cast<const uint8_t*>(w1);
+  a.stride1 = d1->shard_stride_bytes;
+  a.rows1 = (int)d1->rows_per_shard;
+  a.w2 = static_cast<const uint8_t*>(w2);
+  a.stride2 = d2->shard_stride_bytes;
+  a.K2 = (int)d2->k_per_shard;
+  a.x = x;
+  a.mid = mid;
+  a.mid2 = mid2;
+  a.n_q = d1->shape.n_q_heads;
+  a.n_kv = d1->shape.n_kv_heads;
+  a.hd = d1->shape.head_dim;
+  a.residual = res;
+  a.y = y;
+  a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sk_bytes() + ticket_bytes(a.d));
+  a.sync = fused_sync(ws);
+  a.err = tc_error_word();
+  if (!a.err) return TP_ERR_CUDA;
+  return launch_fused(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
 bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {
   if (a.d != b.d || a.t != b.t || a.wtype != b.wtype) return false;
   if (mlp) return a.ffn == b.ffn;
@@ -474,6 +519,9 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
     return TP_ERR_ALIGN;
   if (!ws || ws_bytes < tp_workspace_bytes(&gu->shape, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
+  if (pick_fused(flags, gu, dn, M))
+    return run_fused(FUSED_MLP, gu, gu_w, dn, dn_w, static_cast<const bf16*>(x), static_cast<const bf16*>(residual),
+                     M, static_cast<bf16*>(y), static_cast<bf16*>(h_out), static_cast<bf16*>(h_out), ws, flags, s);
   st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags,
                   ws);
   if (st != TP_OK) return st;
@@ -500,6 +548,9 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
   const tp_shape& sh = qkv->shape;
   if (!ws || ws_bytes < tp_workspace_bytes(&sh, M, flags)) return TP_ERR_WORKSPACE;
   cudaStream_t s = S(stream);
+  if (pick_fused(flags, qkv, o, M))
+    return run_fused(FUSED_PROJ, qkv, qkv_w, o, o_w, static_cast<const bf16*>(x), static_cast<const bf16*>(residual),
+                     M, static_cast<bf16*>(y), static_cast<bf16*>(qkv_out), static_cast<bf16*>(o_in), ws, flags, s);
   st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags,
                   ws);
   if (st != TP_OK) return st;

@@ -1,0 +1,584 @@
+// Fused decode block: one persistent tcgen05 launch per tensor-parallel block.
+//
+// The block is the pages' column-parallel first linear followed by the row-parallel second
+// linear whose shard partials are summed ("The Tensor-Parallel Shard Group",
+// scalablesystem.dev; Y = [XA_1 ... XA_t], Z = sum_k Y_k B_k, "Tensor Parallelism
+// (Megatron-Style)", arunshar.com).  For decode (M <= 64 tokens, one token tile) both
+// halves are weight streams, so they run as one stream of work items in one launch:
+//
+//   items [0, t*n_rt1)            stage 1: (shard s, 128 packed rows) of the first linear
+//                                 -> SwiGLU h, or QKV plus the one-token attention o_in
+//   items [t*n_rt1, + t*n_rt2)    stage 2: (shard s, 128 output rows) of the second linear
+//                                 -> fp32 partial P_s of that row tile
+//
+// Items are taken in that order from one atomic counter (each CTA's first item is its
+// block index, so its weights start streaming before the previous kernel has finished).
+// A stage-2 item of shard s needs the whole stage-1 output of shard s: its producer issues
+// the weight tiles ahead, then waits (bounded) until shard s's stage-1 count is complete.
+// The last of the t shard items of a row tile (ticket) folds the t partials in shard
+// order, adds the residual and writes y: the same left fold, bit for bit, as the separate
+// fold kernel.  No CTA idles while another finishes a second wave of one kernel, and no
+// launch gap separates the halves or the fold.
+//
+// Warp roles per CTA (one CTA per SM): warps 0-3 epilogue, warp 4 TMA producer (and the
+// scheduler), warp 5 MMA issuer.  Every wait is bounded in time; on expiry the kernel
+// records the device error word, drains, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "fused.h"
+#include "tc.h"
+#include "tc_ptx.cuh"
+
+namespace tpx {
+using namespace tc;
+
+namespace {
+
+constexpr int FBM = 128, FBK = 64, kRing = 8;
+constexpr int kProducer = 4, kMma = 5;
+// sync words (all zero between launches)
+constexpr int kSyncItem = 0, kSyncExit = 1, kSyncDone = 8, kSyncTicket = 128;
+
+template <int BN>
+struct FCfg {
+  static constexpr int kABytes = FBM * FBK * 2;
+  static constexpr int kBBytes = BN * FBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
+  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 1024;
+};
+
+struct FItem {
+  int stage, s, rt, nkb;
+};
+
+__device__ __forceinline__ FItem fdecode(const FusedArgs& a, int i) {
+  const int n_rt1 = a.rows1 / FBM, n1 = a.t * n_rt1, n_rt2 = a.d / FBM;
+  FItem f;
+  if (i < n1) {
+    f.stage = 1;
+    f.s = i / n_rt1;
+    f.rt = i % n_rt1;
+    f.nkb = a.d / FBK;
+  } else {
+    const int j = i - n1;
+    f.stage = 2;
+    f.s = j / n_rt2;
+    f.rt = j % n_rt2;
+    f.nkb = a.K2 / FBK;
+  }
+  return f;
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Generic-proxy global writes (h, o_in) are read by other CTAs' TMA (async proxy).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void raise(unsigned* err, unsigned code, volatile int* abort_flag) {
+  atomicExch(err, code);
+  *abort_flag = 1;
+}
+
+// Wait until shard s's stage-1 items are all done (bounded, ~2 s).
+__device__ bool wait_stage1(const FusedArgs& a, int s, volatile int* abort_flag) {
+  const unsigned target = (unsigned)(a.rows1 / FBM);
+  const unsigned* cnt = a.sync + kSyncDone + s;
+  if (ld_acquire(cnt) < target) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; ld_acquire(cnt) < target; ++i) {
+      if (*abort_flag) return false;
+      if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+        raise(a.err, 21, abort_flag);
+        return false;
+      }
+      __nanosleep(32);
+    }
+  }
+  fence_proxy_async_global();
+  return true;
+}
+
+// Stage-1 epilogue for one 16-token chunk of tile row p (packed row of shard s).
+template <int KIND>
+__device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, int mf, const float (&v)[16]) {
+  if (KIND == FUSED_MLP) {
+    // rows come as [8 gate | 8 up] blocks: the up value of row p sits 8 lanes further on
+    float u[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) u[j] = __shfl_down_sync(0xffffffffu, v[j], 8);
+    if ((p & 15) < 8) {
+      const int ldh = a.t * (a.rows1 / 2);
+      const int f = s * (a.rows1 / 2) + (p >> 4) * 8 + (p & 7);
+      uint16_t* h = reinterpret_cast<uint16_t*>(a.mid);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (mf + j < a.M) h[(size_t)(mf + j) * ldh + f] = f2bf(silu_f(v[j]) * u[j]);
+    }
+  } else {
+    // qkv column s*rows1 + p; a v row also becomes o_in for every q head of its group
+    const int ldq = a.t * a.rows1, nqs = a.n_q / a.t, nkvs = a.n_kv / a.t, G = a.n_q / a.n_kv;
+    const int vb = (nqs + nkvs) * a.hd;
+    uint16_t* q = reinterpret_cast<uint16_t*>(a.mid);
+    uint16_t* o = reinterpret_cast<uint16_t*>(a.mid2);
+    const int ldo = a.n_q * a.hd;
+    const bool vrow = p >= vb;
+    const int j = vrow ? (p - vb) / a.hd : 0, e = vrow ? (p - vb) % a.hd : 0;
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj) {
+      const int m = mf + jj;
+      if (m >= a.M) break;
+      const uint16_t b = f2bf(v[jj]);
+      q[(size_t)m * ldq + (size_t)s * a.rows1 + p] = b;
+      if (vrow)
+        for (int g = 0; g < G; ++g) o[(size_t)m * ldo + (size_t)(s * nqs + j * G + g) * a.hd + e] = b;
+    }
+  }
+}
+
+// The last shard item of row tile rt folds: y = bf16(((P_0 + P_1) + ... + P_{t-1}) + residual),
+// four rows of one token per thread per step.
+__device__ __forceinline__ void fold_tile(const FusedArgs& a, int rt) {
+  const int r4 = (threadIdx.x & 31) * 4;
+  const size_t MD = (size_t)a.M * a.d;
+  for (int m = threadIdx.x >> 5; m < a.M; m += 4) {
+    const size_t base = (size_t)m * a.d + (size_t)rt * FBM + r4;
+    float4 acc = __ldcg(reinterpret_cast<const float4*>(a.partials + base));
+#pragma unroll
+    for (int s = 1; s < 8; ++s) {
+      if (s < a.t) {
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partials + (size_t)s * MD + base));
+        acc.x += p.x;
+        acc.y += p.y;
+        acc.z += p.z;
+        acc.w += p.w;
+      }
+    }
+    if (a.residual) {
+      const uint2 r = *reinterpret_cast<const uint2*>(a.residual + base);
+      acc.x += bf16_lo(r.x);
+      acc.y += bf16_hi(r.x);
+      acc.z += bf16_lo(r.y);
+      acc.w += bf16_hi(r.y);
+    }
+    uint2 o;
+    o.x = (uint32_t)f2bf(acc.x) | ((uint32_t)f2bf(acc.y) << 16);
+    o.y = (uint32_t)f2bf(acc.z) | ((uint32_t)f2bf(acc.w) << 16);
+    *reinterpret_cast<uint2*>(a.y + base) = o;
+  }
+}
+
+template <int BN, int KIND>
+__global__ void __launch_bounds__(192, 1)
+    fused_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
+                 const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, FusedArgs a) {
+  using C = FCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;                            // S x [128 rows x 64] bf16, SW128
+  uint8_t* sB = smem + (size_t)S * C::kABytes;   // S x [BN rows x 64] bf16, SW128
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], ifull[kRing], iempty[kRing], drain
+  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kRing);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 2);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
+                 tempty0 = smem_u32(bars + 2 * S + 2), ifull0 = smem_u32(bars + 2 * S + 4),
+                 iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n1 = a.t * (a.rows1 / FBM), ntot = n1 + a.t * (a.d / FBM);
+
+  // fail fast after a bounded wait has given up (the error word is cleared by tp_sync)
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = *reinterpret_cast<volatile unsigned*>(a.err) != 0u;
+  __syncthreads();
+  if (s_skip) return;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull0 + 8 * i, 1);
+      mbar_init(tempty0 + 8 * i, 4);  // one arrival per epilogue warp
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(ifull0 + 8 * i, 1);
+      mbar_init(iempty0 + 8 * i, 5);  // the MMA thread + one lane per epilogue warp
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *mma_consumed = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kProducer && lane == 0) {
+    tma_prefetch_desc(&tmA1);
+    tma_prefetch_desc(&tmB1);
+    tma_prefetch_desc(&tmA2);
+    tma_prefetch_desc(&tmB2);
+  }
+  if (warp == kMma) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  int issued = 0;
+
+  griddep_launch_dependents();
+  if (warp == kProducer) {
+    if (lane == 0) {
+      const uint64_t pol_w = l2_evict_first(), pol_x = l2_evict_last();
+      int q = 0;  // items published
+      bool ok = true;
+      auto publish = [&](int id) {
+        const int r = q % kRing;
+        if (q >= kRing && !mbar_wait(iempty0 + 8 * r, ((q / kRing) - 1) & 1)) {
+          raise(a.err, 22, abort_flag);
+          ok = false;
+          return;
+        }
+        ring[r] = id;
+        mbar_arrive(ifull0 + 8 * r);
+        ++q;
+      };
+      auto load_a = [&](const FItem& f, int kb, int st) {
+        const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes), bar = full0 + 8 * st;
+        if (f.stage == 1)
+          tma_load_3d_hint(dst, &tmA1, kb * FBK, f.rt * FBM, f.s, bar, pol_w);
+        else
+          tma_load_3d_hint(dst, &tmA2, kb * FBK, f.rt * FBM, f.s, bar, pol_w);
+      };
+      auto load_b = [&](const FItem& f, int kb, int st) {
+        const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes), bar = full0 + 8 * st;
+        if (f.stage == 1)
+          tma_load_2d_hint(dst, &tmB1, kb * FBK, 0, bar, pol_x);
+        else
+          tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * FBK, 0, bar, pol_x);
+      };
+      // first item (static): its first stages of weights go out before the previous kernel ends
+      int item = blockIdx.x;
+      FItem f = fdecode(a, item);
+      const int pre = f.nkb < S ? f.nkb : S;
+      for (int kb = 0; kb < pre; ++kb) {
+        mbar_expect_tx(full0 + 8 * kb, C::kABytes);
+        load_a(f, kb, kb);
+      }
+      griddep_wait();
+      publish(item);
+      if (ok && f.stage == 2) ok = wait_stage1(a, f.s, abort_flag);
+      if (ok) {
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_arrive_expect_tx(full0 + 8 * kb, C::kBBytes);
+          load_b(f, kb, kb);
+        }
+        issued = pre;
+      }
+      for (int kb = pre; ok && kb < f.nkb; ++kb) {
+        const int st = issued % S;
+        if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+          raise(a.err, 23, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+        load_a(f, kb, st);
+        load_b(f, kb, st);
+        ++issued;
+      }
+      // then items from the shared counter, in order: stage 1 of every shard, then stage 2
+      while (ok && !*abort_flag) {
+        item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
+        if (item >= ntot) break;
+        f = fdecode(a, item);
+        publish(item);
+        if (!ok) break;
+        int kb = 0;
+        if (f.stage == 2 && ld_acquire(a.sync + kSyncDone + f.s) < (unsigned)(a.rows1 / FBM)) {
+          // weights ahead (their stages were freed by earlier items), then the activations
+          const int la = f.nkb < S ? f.nkb : S;
+          for (; kb < la; ++kb) {
+            const int st = issued % S;
+            if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+              raise(a.err, 24, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+            load_a(f, kb, st);
+            ++issued;
+          }
+          if (ok) ok = wait_stage1(a, f.s, abort_flag);
+          if (!ok) break;
+          for (int j = 0; j < la; ++j) load_b(f, j, (issued - la + j) % S);
+        } else if (f.stage == 2) {
+          fence_proxy_async_global();
+        }
+        for (; kb < f.nkb; ++kb) {
+          const int st = issued % S;
+          if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+            raise(a.err, 25, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+          load_a(f, kb, st);
+          load_b(f, kb, st);
+          ++issued;
+        }
+      }
+      if (ok) publish(-1);
+    }
+  } else if (warp == kMma) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(FBM, BN);
+      int q = 0, it = 0, consumed = 0;
+      while (!*abort_flag) {
+        const int r = q % kRing;
+        if (!mbar_wait(ifull0 + 8 * r, (q / kRing) & 1)) {
+          raise(a.err, 26, abort_flag);
+          break;
+        }
+        const int id = ring[r];
+        mbar_arrive(iempty0 + 8 * r);
+        ++q;
+        if (id < 0) break;
+        const FItem f = fdecode(a, id);
+        const int acc = it & 1;
+        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) {
+          raise(a.err, 27, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kb = 0; kb < f.nkb; ++kb) {
+          const int st = consumed % S;
+          if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1)) {
+            raise(a.err, 28, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)st * C::kBBytes);
+#pragma unroll
+          for (int k = 0; k < FBK / 16; ++k)
+            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+          mma_commit(empty0 + 8 * st);
+          ++consumed;
+        }
+        if (!ok) break;
+        mma_commit(tfull0 + 8 * acc);
+        ++it;
+      }
+      *mma_consumed = consumed;
+      mma_commit(drain_bar);
+      if (!mbar_wait(drain_bar, 0)) raise(a.err, 29, abort_flag);
+    }
+  } else {
+    // epilogue warps 0..3: global writes only after the grids this one depends on
+    griddep_wait();
+    const int r = warp * 32 + lane;  // row inside the 128-row tile
+    int q = 0, it = 0;
+    while (true) {
+      const int rr = q % kRing;
+      if (!__all_sync(0xffffffffu, mbar_wait(ifull0 + 8 * rr, (q / kRing) & 1))) {
+        raise(a.err, 30, abort_flag);
+        break;
+      }
+      const int id = ring[rr];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(iempty0 + 8 * rr);
+      ++q;
+      if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const FItem f = fdecode(a, id);
+      const int acc = it & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
+        raise(a.err, 31, abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
+      const int p = f.rt * FBM + r;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        float v[16];
+        tmem_ld16(tb + c0, v);
+        tmem_ld_wait();
+        if (f.stage == 1) {
+          stage1_chunk<KIND>(a, f.s, p, c0, v);
+        } else {
+          float* P = a.partials + (size_t)f.s * a.M * a.d + p;
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            if (c0 + j < a.M) P[(size_t)(c0 + j) * a.d] = v[j];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      ++it;
+      // make this item's stores visible, then count it (stage 1) or take the tile's ticket (stage 2)
+      __threadfence();
+      if (f.stage == 1) fence_proxy_async_global();
+      epi_bar();
+      if (f.stage == 1) {
+        if (threadIdx.x == 0) red_release_add(a.sync + kSyncDone + f.s, 1u);
+      } else {
+        if (threadIdx.x == 0) {
+          const unsigned old = atomicAdd(a.sync + kSyncTicket + f.rt, 1u);
+          const int last = old == (unsigned)(a.t - 1);
+          if (last) a.sync[kSyncTicket + f.rt] = 0u;  // every shard has arrived: reset for the next launch
+          __threadfence();
+          *last_flag = last;
+        }
+        epi_bar();
+        if (*last_flag) fold_tile(a, f.rt);
+      }
+    }
+  }
+
+  __syncthreads();
+  // drain: wait (bounded) for any TMA copy issued but never consumed
+  if (warp == kProducer && lane == 0) {
+    for (int qq = *mma_consumed; qq < issued; ++qq)
+      if (!mbar_wait(full0 + 8 * (qq % S), (qq / S) & 1)) {
+        atomicExch(a.err, 32u);
+        break;
+      }
+  }
+  __syncthreads();
+  if (warp == kMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+  // the last CTA out resets the scheduler words for the next launch
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(a.sync + kSyncExit, 1u) == gridDim.x - 1) {
+      a.sync[kSyncItem] = 0u;
+      for (int s = 0; s < 8; ++s) a.sync[kSyncDone + s] = 0u;
+      if (*reinterpret_cast<volatile unsigned*>(a.err) != 0u)
+        for (int rt = 0; rt < a.d / FBM; ++rt) a.sync[kSyncTicket + rt] = 0u;
+      a.sync[kSyncExit] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace
+
+bool fused_supported(int rows1, int d, int K2, int M, int t) {
+  return M > 0 && M <= kFusedMaxM && t >= 1 && t <= 8 && rows1 % FBM == 0 && rows1 > 0 && d % FBM == 0 &&
+         d > 0 && K2 % FBK == 0 && K2 > 0 && fused_sync_words(d) <= kTcMaxStreamkItems - 64;
+}
+
+template <int BN, int KIND>
+static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
+  using C = FCfg<BN>;
+  EncodeTiled enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  CUtensorMap tm[4];
+  const cuuint32_t es3[3] = {1, 1, 1}, es2[2] = {1, 1};
+  {  // stage-1 weights {K1 = d, rows1, t}
+    const cuuint64_t dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.rows1, (cuuint64_t)a.t};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.d * 2, (cuuint64_t)a.stride1};
+    const cuuint32_t box[3] = {FBK, FBM, 1};
+    if (enc(&tm[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w1), dims, strides, box, es3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {  // x [M, d]
+    const cuuint64_t dims[2] = {(cuuint64_t)a.d, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.d * 2};
+    const cuuint32_t box[2] = {FBK, BN};
+    if (enc(&tm[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), dims, strides, box, es2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {  // stage-2 weights {K2, rows2 = d, t}
+    const cuuint64_t dims[3] = {(cuuint64_t)a.K2, (cuuint64_t)a.d, (cuuint64_t)a.t};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K2 * 2, (cuuint64_t)a.stride2};
+    const cuuint32_t box[3] = {FBK, FBM, 1};
+    if (enc(&tm[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w2), dims, strides, box, es3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {  // stage-2 activations [M, t*K2] (h or o_in)
+    const cuuint64_t dims[2] = {(cuuint64_t)a.t * a.K2, (cuuint64_t)a.M};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.t * a.K2 * 2};
+    const cuuint32_t box[2] = {FBK, BN};
+    if (enc(&tm[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.mid2, dims, strides, box, es2,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(fused_kernel<BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int ntot = a.t * (a.rows1 / FBM) + a.t * (a.d / FBM);
+  const int grid = ntot < sms ? ntot : sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  // CTAs wait on one another's items: all of them must be resident together
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND>, tm[0], tm[1], tm[2], tm[3], a);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int KIND>
+static cudaError_t fused_bn(const FusedArgs& a, cudaStream_t st, bool pdl) {
+  if (a.M <= 16) return fused_go<16, KIND>(a, st, pdl);
+  if (a.M <= 32) return fused_go<32, KIND>(a, st, pdl);
+  return fused_go<64, KIND>(a, st, pdl);
+}
+
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
+  if (!fused_supported(a.rows1, a.d, a.K2, a.M, a.t) || !a.err || !a.sync || !a.partials)
+    return cudaErrorInvalidValue;
+  if ((reinterpret_cast<uintptr_t>(a.w1) | reinterpret_cast<uintptr_t>(a.w2) | reinterpret_cast<uintptr_t>(a.x) |
+       reinterpret_cast<uintptr_t>(a.mid2)) & 15)
+    return cudaErrorInvalidValue;
+  return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP>(a, st, pdl) : fused_bn<FUSED_PROJ>(a, st, pdl);
+}
+
+}  // namespace tpx

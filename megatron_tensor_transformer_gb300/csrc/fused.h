@@ -1,0 +1,46 @@
+// Host-side interface of the fused decode block kernel: one persistent tcgen05 launch runs a
+// whole tensor-parallel block (column-parallel first linear, then row-parallel second linear
+// with its shard fold) for up to 64 tokens.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tpx {
+
+enum FusedKind {
+  FUSED_MLP = 0,  // stage 1 = gate/up + SwiGLU -> h; stage 2 = down over h
+  FUSED_PROJ = 1  // stage 1 = QKV -> qkv (+ the one-token attention into o_in); stage 2 = o_proj over o_in
+};
+
+struct FusedArgs {
+  int kind;
+  int t, M, d;
+  // stage 1 (column-parallel): per-shard packed matrix [rows1, K1 = d]
+  const uint8_t* w1;
+  uint64_t stride1;
+  int rows1;
+  // stage 2 (row-parallel): per-shard packed matrix [rows2 = d, K2]
+  const uint8_t* w2;
+  uint64_t stride2;
+  int K2;
+  const __nv_bfloat16* x;        // [M, d]
+  __nv_bfloat16* mid;            // stage-1 output: h [M, t*rows1/2] or qkv [M, t*rows1]
+  __nv_bfloat16* mid2;           // stage-2 input [M, t*K2]: h (== mid) or o_in
+  int n_q, n_kv, hd;             // FUSED_PROJ head geometry (whole model)
+  const __nv_bfloat16* residual; // nullable [M, d]
+  __nv_bfloat16* y;              // [M, d]
+  float* partials;               // [t][M][d] fp32
+  unsigned* sync;                // zeroed words: item counter, exit counter, per-shard counts, tile tickets
+  unsigned* err;                 // device error word (fail fast, and set when a bounded wait gives up)
+};
+
+constexpr int kFusedMaxM = 64;
+// words of the sync area the fused kernel uses: 128 + one ticket per 128-row output tile
+inline int fused_sync_words(int d) { return 128 + d / 128; }
+
+// Whether the fused kernel supports this block (bf16 weights, 128-row / 64-k tiles, M <= 64).
+bool fused_supported(int rows1, int d, int K2, int M, int t);
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl);
+
+}  // namespace tpx

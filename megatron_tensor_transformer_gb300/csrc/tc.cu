@@ -626,11 +626,7 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
 
 // ---------------------------------------------------------------- host side
 
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-static EncodeTiled encode_fn() {
+EncodeTiled encode_fn() {
   static EncodeTiled fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -683,6 +679,20 @@ cudaError_t launch_e4m3_decode(const void* codes, void* out, int n, cudaStream_t
   e4m3_decode_kernel<<<(n4 + 255) / 256, 256, 0, st>>>(static_cast<const uint32_t*>(codes), static_cast<uint2*>(out), n4);
   note_launch();
   return cudaGetLastError();
+}
+
+unsigned* tc_error_word() {
+  static std::mutex mu;
+  static unsigned* cache[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_tc_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned*>(p);
+  }
+  return cache[dev];
 }
 
 unsigned tc_take_device_error() {

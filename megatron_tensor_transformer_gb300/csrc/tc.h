@@ -1,5 +1,6 @@
 // Host-side interface of the tcgen05 weight-streaming GEMM (weights on the MMA's M side).
 #pragma once
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -57,5 +58,14 @@ cudaError_t launch_bounded_wait_selftest(int timeout_us, cudaStream_t st);
 cudaError_t launch_e4m3_decode(const void* codes, void* out, int n, cudaStream_t st);
 // Device error word set by a bounded wait that gave up (0 = none); read and cleared.
 unsigned tc_take_device_error();
+// Device address of that error word on the current device (resolved once per device), for
+// kernels in other translation units; nullptr if it cannot be resolved.
+unsigned* tc_error_word();
+
+// cuTensorMapEncodeTiled, resolved through the runtime's driver entry point (nullptr if absent).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encode_fn();
 
 }  // namespace tpx

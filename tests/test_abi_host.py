@@ -115,7 +115,7 @@ def test_argument_errors_before_launch():
     sh = tpx.make_shape(4096, ffn=14336, t=8)
     gu, dn = tpx.tp_describe(sh, tpx.TP_W_GATE_UP), tpx.tp_describe(sh, tpx.TP_W_DOWN)
     assert _call_mlp(gu, dn, M=-1) == tpx.TP_ERR_INVALID_ARG
-    assert _call_mlp(gu, dn, flags=0x80) == tpx.TP_ERR_INVALID_ARG
+    assert _call_mlp(gu, dn, flags=0x100) == tpx.TP_ERR_INVALID_ARG              # unknown flag bit
     assert _call_mlp(gu, dn, ws=None, ws_bytes=0) == tpx.TP_ERR_WORKSPACE
     need = tpx.tp_workspace_bytes(sh, 8)
     assert _call_mlp(gu, dn, ws_bytes=need - 1) == tpx.TP_ERR_WORKSPACE
