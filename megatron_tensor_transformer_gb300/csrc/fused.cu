@@ -147,35 +147,48 @@ __device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, i
   }
 }
 
-// The last shard item of row tile rt folds: y = bf16(((P_0 + P_1) + ... + P_{t-1}) + residual),
-// four rows of one token per thread per step.
+// The last shard item of row tile rt folds: y = bf16(((P_0 + P_1) + ... + P_{t-1}) + residual).
+// Each thread takes four rows of four tokens per step and issues all 4 x t loads before the
+// adds, so a fold of 64 tokens costs a few L2 round trips instead of one per token group.
 __device__ __forceinline__ void fold_tile(const FusedArgs& a, int rt) {
-  const int r4 = (threadIdx.x & 31) * 4;
+  const int r4 = (threadIdx.x & 31) * 4, w = threadIdx.x >> 5;
   const size_t MD = (size_t)a.M * a.d;
-  for (int m = threadIdx.x >> 5; m < a.M; m += 4) {
-    const size_t base = (size_t)m * a.d + (size_t)rt * FBM + r4;
-    float4 acc = __ldcg(reinterpret_cast<const float4*>(a.partials + base));
+  for (int m0 = 4 * w; m0 < a.M; m0 += 16) {
+    float4 p[4][8];
 #pragma unroll
-    for (int s = 1; s < 8; ++s) {
-      if (s < a.t) {
-        const float4 p = __ldcg(reinterpret_cast<const float4*>(a.partials + (size_t)s * MD + base));
-        acc.x += p.x;
-        acc.y += p.y;
-        acc.z += p.z;
-        acc.w += p.w;
+    for (int u = 0; u < 4; ++u) {
+      const size_t base = (size_t)(m0 + u) * a.d + (size_t)rt * FBM + r4;
+#pragma unroll
+      for (int s = 0; s < 8; ++s)
+        if (m0 + u < a.M && s < a.t) p[u][s] = __ldcg(reinterpret_cast<const float4*>(a.partials + s * MD + base));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int m = m0 + u;
+      if (m >= a.M) break;
+      const size_t base = (size_t)m * a.d + (size_t)rt * FBM + r4;
+      float4 acc = p[u][0];
+#pragma unroll
+      for (int s = 1; s < 8; ++s) {
+        if (s < a.t) {
+          acc.x += p[u][s].x;
+          acc.y += p[u][s].y;
+          acc.z += p[u][s].z;
+          acc.w += p[u][s].w;
+        }
       }
+      if (a.residual) {
+        const uint2 r = *reinterpret_cast<const uint2*>(a.residual + base);
+        acc.x += bf16_lo(r.x);
+        acc.y += bf16_hi(r.x);
+        acc.z += bf16_lo(r.y);
+        acc.w += bf16_hi(r.y);
+      }
+      uint2 o;
+      o.x = (uint32_t)f2bf(acc.x) | ((uint32_t)f2bf(acc.y) << 16);
+      o.y = (uint32_t)f2bf(acc.z) | ((uint32_t)f2bf(acc.w) << 16);
+      *reinterpret_cast<uint2*>(a.y + base) = o;
     }
-    if (a.residual) {
-      const uint2 r = *reinterpret_cast<const uint2*>(a.residual + base);
-      acc.x += bf16_lo(r.x);
-      acc.y += bf16_hi(r.x);
-      acc.z += bf16_lo(r.y);
-      acc.w += bf16_hi(r.y);
-    }
-    uint2 o;
-    o.x = (uint32_t)f2bf(acc.x) | ((uint32_t)f2bf(acc.y) << 16);
-    o.y = (uint32_t)f2bf(acc.z) | ((uint32_t)f2bf(acc.w) << 16);
-    *reinterpret_cast<uint2*>(a.y + base) = o;
   }
 }
 
@@ -552,14 +565,15 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   cfg.blockDim = dim3(192);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  // No cooperative launch: it would keep this grid from starting while the previous kernel
+  // drains.  CTAs do wait on one another's items, but the grid is at most one CTA per SM and
+  // the only CTAs that can hold an SM are those of kernels that finish without waiting on this
+  // one, so every CTA becomes resident; each wait is bounded in any case.
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
-  // CTAs wait on one another's items: all of them must be resident together
-  attr[1].id = cudaLaunchAttributeCooperative;
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND>, tm[0], tm[1], tm[2], tm[3], a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
