@@ -393,12 +393,12 @@ unsigned* fused_sync(void* ws) {
                                      (size_t)kTcMaxStreamkItems * 4) + 64;
 }
 
-// One persistent launch for the whole block (decode token counts, bf16 weights), unless the
-// flags ask for separate launches or for the mma.sync kernels.
+// One persistent launch for the whole block (decode token counts, bf16 or e4m3 weights), unless
+// the flags ask for separate launches or for the mma.sync kernels.
 bool pick_fused(uint32_t flags, const tp_packed_desc* d1, const tp_packed_desc* d2, int M) {
   if (flags & (TP_F_UNFUSED_REDUCE | TP_F_KERNEL_SKINNY | TP_F_SPLIT_BLOCK)) return false;
-  if (d1->wtype != TP_BF16) return false;
-  return fused_supported((int)d1->rows_per_shard, d1->shape.d, (int)d2->k_per_shard, M, d1->shape.t);
+  return fused_supported((int)d1->rows_per_shard, d1->shape.d, (int)d2->k_per_shard, M, d1->shape.t,
+                         d1->wtype == TP_FP8_E4M3);
 }
 
 tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp_packed_desc* d2, const void* w2,
@@ -409,8 +409,11 @@ tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp
   a.t = d1->shape.t;
   a.M = M;
   a.d = d1->shape.d;
+  a.fp8 = d1->wtype == TP_FP8_E4M3;
   a.w1 = static_cast<const uint8_t*>(w1);
   a.stride1 = d1->shard_stride_bytes;
+  a.scales1 = d1->scales_offset;
+  a.scales2 = d2->scales_offset;
   a.rows1 = (int)d1->rows_per_shard;
   a.w2 = static_cast<const uint8_t*>(w2);
   a.stride2 = d2->shard_stride_bytes;

@@ -36,38 +36,60 @@ using namespace tc;
 namespace {
 
 constexpr int FBM = 128, FBK = 64, kRing = 8;
-constexpr int kProducer = 4, kMma = 5;
+constexpr int kProducer = 4, kMma = 5, kProducerB = 14;
 // sync words (all zero between launches)
 constexpr int kSyncItem = 0, kSyncExit = 1, kSyncDone = 8, kSyncTicket = 128;
 
-template <int BN>
+// bf16 weights: each stage holds one 64-wide k-block, the 128 x 64 bf16 weight tile (128-byte
+// swizzle) the MMA reads from shared memory.  e4m3 weights: each stage holds a 128-wide k-block,
+// the 128 x 128 e4m3 tile as TMA brings it (128-byte swizzle: 128 contiguous bytes per row, as
+// for bf16; 64-byte rows at the weights' row stride read HBM at about half the rate), and two
+// 64-wide activation tiles.  Converter warps widen the tile, exactly, to bf16 in tensor memory
+// (one of kASlots 64-column A slots from column kACol0) and the MMA reads A from there.  A warp
+// may only address one quarter of the TMEM lanes, so the converters come as two warps per
+// quarter, each widening one 64-wide half of its 32 rows.  With e4m3 weights the activation
+// tiles travel in a ring of their own (kSB slots, issued by a second producer warp and freed
+// by the MMA), so a weight stage is free again as soon as the converters have read it: the
+// weight ring is then almost entirely in flight from HBM.
+template <int BN, bool FP8>
 struct FCfg {
-  static constexpr int kABytes = FBM * FBK * 2;
-  static constexpr int kBBytes = BN * FBK * 2;
+  static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per stage
+  static constexpr int kABytes = FP8 ? FBM * kKB : FBM * kKB * 2;
+  static constexpr int kBSub = BN * FBK * 2;               // one 64-wide activation tile
+  static constexpr int kBBytes = kBSub * (kKB / FBK);
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kStages = (200 * 1024) / kStageBytes > 8 ? 8 : (200 * 1024) / kStageBytes;
-  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 1024;
+  static constexpr int kSB = FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0;  // activation ring (e4m3 only)
+  static constexpr int kMaxStages = FP8 ? 10 : 8;
+  static constexpr int kRingBytes = FP8 ? 200 * 1024 - kSB * kBBytes : 200 * 1024;
+  static constexpr int kUnitBytes = FP8 ? kABytes : kStageBytes;
+  static constexpr int kStages = kRingBytes / kUnitBytes > kMaxStages ? kMaxStages : kRingBytes / kUnitBytes;
+  static constexpr int kBSlots = FP8 ? kSB : kStages;  // activation tiles held in shared memory
+  static constexpr int kASlots = 6, kACol0 = 128, kASlotCols = kKB / 2;
+  static constexpr int kTmemCols = FP8 ? 512 : (2 * BN < 32 ? 32 : 2 * BN);
+  static constexpr int kConvWarps = FP8 ? 8 : 0;
+  // converter warps from warp 6; e4m3: then the activation producer (warp 14)
+  static constexpr int kThreads = 192 + 32 * kConvWarps + (FP8 ? 32 : 0);
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + (size_t)kBSlots * kBBytes + 1024;
 };
 
 struct FItem {
   int stage, s, rt, nkb;
 };
 
-__device__ __forceinline__ FItem fdecode(const FusedArgs& a, int i) {
+__device__ __forceinline__ FItem fdecode(const FusedArgs& a, int i, int kkb) {
   const int n_rt1 = a.rows1 / FBM, n1 = a.t * n_rt1, n_rt2 = a.d / FBM;
   FItem f;
   if (i < n1) {
     f.stage = 1;
     f.s = i / n_rt1;
     f.rt = i % n_rt1;
-    f.nkb = a.d / FBK;
+    f.nkb = a.d / kkb;
   } else {
     const int j = i - n1;
     f.stage = 2;
     f.s = j / n_rt2;
     f.rt = j % n_rt2;
-    f.nkb = a.K2 / FBK;
+    f.nkb = a.K2 / kkb;
   }
   return f;
 }
@@ -110,6 +132,13 @@ __device__ bool wait_stage1(const FusedArgs& a, int s, volatile int* abort_flag)
   return true;
 }
 
+// e4m3 weights: the fp32 scale of packed row p of shard s in stage 1 or 2 (1 for bf16).
+__device__ __forceinline__ float wscale(const FusedArgs& a, int stage, int s, int p) {
+  if (!a.fp8) return 1.f;
+  const uint8_t* b = stage == 1 ? a.w1 + (size_t)s * a.stride1 + a.scales1 : a.w2 + (size_t)s * a.stride2 + a.scales2;
+  return reinterpret_cast<const float*>(b)[p];
+}
+
 // Stage-1 epilogue for one 16-token chunk of tile row p (packed row of shard s).
 template <int KIND>
 __device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, int mf, const float (&v)[16]) {
@@ -148,22 +177,23 @@ __device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, i
 }
 
 // The last shard item of row tile rt folds: y = bf16(((P_0 + P_1) + ... + P_{t-1}) + residual).
-// Each thread takes four rows of four tokens per step and issues all 4 x t loads before the
+// Each thread takes four rows of U tokens per step and issues all U x t loads before the
 // adds, so a fold of 64 tokens costs a few L2 round trips instead of one per token group.
+template <int U>
 __device__ __forceinline__ void fold_tile(const FusedArgs& a, int rt) {
   const int r4 = (threadIdx.x & 31) * 4, w = threadIdx.x >> 5;
   const size_t MD = (size_t)a.M * a.d;
-  for (int m0 = 4 * w; m0 < a.M; m0 += 16) {
-    float4 p[4][8];
+  for (int m0 = U * w; m0 < a.M; m0 += 4 * U) {
+    float4 p[U][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const size_t base = (size_t)(m0 + u) * a.d + (size_t)rt * FBM + r4;
 #pragma unroll
       for (int s = 0; s < 8; ++s)
         if (m0 + u < a.M && s < a.t) p[u][s] = __ldcg(reinterpret_cast<const float4*>(a.partials + s * MD + base));
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int m = m0 + u;
       if (m >= a.M) break;
       const size_t base = (size_t)m * a.d + (size_t)rt * FBM + r4;
@@ -192,26 +222,30 @@ __device__ __forceinline__ void fold_tile(const FusedArgs& a, int rt) {
   }
 }
 
-template <int BN, int KIND>
-__global__ void __launch_bounds__(192, 1)
+template <int BN, int KIND, bool FP8>
+__global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                  const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, FusedArgs a) {
-  using C = FCfg<BN>;
+  using C = FCfg<BN, FP8>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;                            // S x [128 rows x 64] bf16, SW128
-  uint8_t* sB = smem + (size_t)S * C::kABytes;   // S x [BN rows x 64] bf16, SW128
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)S * C::kStageBytes);
-  // bars: full[S], empty[S], tfull[2], tempty[2], ifull[kRing], iempty[kRing], drain
-  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1);
+  uint8_t* sA = smem;                            // S x [128 rows x 64] weights (bf16 SW128 or e4m3 SW64)
+  uint8_t* sB = smem + (size_t)S * C::kABytes;   // kBSlots x [BN rows x kKB] bf16, SW128 tiles of 64
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)C::kBSlots * C::kBBytes);
+  // bars: full[S], empty[S], tfull[2], tempty[2], ifull[kRing], iempty[kRing], drain, afull[kASlots],
+  // aempty[kASlots], fullB[kSB], emptyB[kSB]
+  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1 + 2 * C::kASlots + 2 * C::kSB);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 2);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  int* conv_consumed = reinterpret_cast<int*>(tmem_slot + 4);  // e4m3: weight stages the converters took
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
                  tempty0 = smem_u32(bars + 2 * S + 2), ifull0 = smem_u32(bars + 2 * S + 4),
-                 iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing);
+                 iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing),
+                 afull0 = drain_bar + 8, aempty0 = drain_bar + 8 + 8 * C::kASlots,
+                 fullB0 = aempty0 + 8 * C::kASlots, emptyB0 = fullB0 + 8 * C::kSB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n1 = a.t * (a.rows1 / FBM), ntot = n1 + a.t * (a.d / FBM);
 
@@ -224,7 +258,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, FP8 ? C::kConvWarps : 1);  // e4m3: freed by the converters
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
@@ -232,12 +266,24 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(ifull0 + 8 * i, 1);
-      mbar_init(iempty0 + 8 * i, 5);  // the MMA thread + one lane per epilogue warp
+      // the MMA thread + one lane per epilogue / converter warp (+ the activation producer)
+      mbar_init(iempty0 + 8 * i, 5 + C::kConvWarps + (FP8 ? 1 : 0));
     }
     mbar_init(drain_bar, 1);
+    if constexpr (FP8) {
+      for (int i = 0; i < C::kASlots; ++i) {
+        mbar_init(afull0 + 8 * i, C::kConvWarps);  // one arrival per converter warp
+        mbar_init(aempty0 + 8 * i, 1);  // tcgen05.commit after the MMAs that read the slot
+      }
+      for (int i = 0; i < C::kSB; ++i) {
+        mbar_init(fullB0 + 8 * i, 1);
+        mbar_init(emptyB0 + 8 * i, 1);  // tcgen05.commit after the MMAs that read the tile
+      }
+    }
     *abort_flag = 0;
     *mma_consumed = 0;
     *last_flag = 0;
+    *conv_consumed = 0;
     fence_mbar_init();
   }
   if (warp == kProducer && lane == 0) {
@@ -254,7 +300,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  int issued = 0;
+  int issued = 0, issuedB = 0;  // weight stages / (e4m3) activation tiles this thread issued
 
   griddep_launch_dependents();
   if (warp == kProducer) {
@@ -276,79 +322,68 @@ __global__ void __launch_bounds__(192, 1)
       auto load_a = [&](const FItem& f, int kb, int st) {
         const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes), bar = full0 + 8 * st;
         if (f.stage == 1)
-          tma_load_3d_hint(dst, &tmA1, kb * FBK, f.rt * FBM, f.s, bar, pol_w);
+          tma_load_3d_hint(dst, &tmA1, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
         else
-          tma_load_3d_hint(dst, &tmA2, kb * FBK, f.rt * FBM, f.s, bar, pol_w);
+          tma_load_3d_hint(dst, &tmA2, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
       };
       auto load_b = [&](const FItem& f, int kb, int st) {
-        const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes), bar = full0 + 8 * st;
-        if (f.stage == 1)
-          tma_load_2d_hint(dst, &tmB1, kb * FBK, 0, bar, pol_x);
-        else
-          tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * FBK, 0, bar, pol_x);
+        const uint32_t bar = full0 + 8 * st;
+        for (int h = 0; h < C::kKB / FBK; ++h) {
+          const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + h * C::kBSub);
+          if (f.stage == 1)
+            tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
+          else
+            tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
+        }
       };
       // first item (static): its first stages of weights go out before the previous kernel ends
       int item = blockIdx.x;
-      FItem f = fdecode(a, item);
-      const int pre = f.nkb < S ? f.nkb : S;
-      for (int kb = 0; kb < pre; ++kb) {
-        mbar_expect_tx(full0 + 8 * kb, C::kABytes);
-        load_a(f, kb, kb);
-      }
-      griddep_wait();
-      publish(item);
-      if (ok && f.stage == 2) ok = wait_stage1(a, f.s, abort_flag);
-      if (ok) {
-        for (int kb = 0; kb < pre; ++kb) {
-          mbar_arrive_expect_tx(full0 + 8 * kb, C::kBBytes);
-          load_b(f, kb, kb);
-        }
-        issued = pre;
-      }
-      for (int kb = pre; ok && kb < f.nkb; ++kb) {
-        const int st = issued % S;
-        if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
-          raise(a.err, 23, abort_flag);
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-        load_a(f, kb, st);
-        load_b(f, kb, st);
-        ++issued;
-      }
-      // then items from the shared counter, in order: stage 1 of every shard, then stage 2
-      while (ok && !*abort_flag) {
-        item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
-        if (item >= ntot) break;
-        f = fdecode(a, item);
-        publish(item);
-        if (!ok) break;
-        int kb = 0;
-        if (f.stage == 2 && ld_acquire(a.sync + kSyncDone + f.s) < (unsigned)(a.rows1 / FBM)) {
-          // weights ahead (their stages were freed by earlier items), then the activations
-          const int la = f.nkb < S ? f.nkb : S;
-          for (; kb < la; ++kb) {
-            const int st = issued % S;
-            if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
-              raise(a.err, 24, abort_flag);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-            load_a(f, kb, st);
-            ++issued;
-          }
-          if (ok) ok = wait_stage1(a, f.s, abort_flag);
-          if (!ok) break;
-          for (int j = 0; j < la; ++j) load_b(f, j, (issued - la + j) % S);
-        } else if (f.stage == 2) {
-          fence_proxy_async_global();
-        }
-        for (; kb < f.nkb; ++kb) {
+      FItem f = fdecode(a, item, C::kKB);
+      if constexpr (FP8) {
+        // weights only: the activation tiles have a producer warp of their own
+        auto issue_w = [&](const FItem& g, int kb) {
           const int st = issued % S;
           if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
-            raise(a.err, 25, abort_flag);
+            raise(a.err, 23, abort_flag);
+            ok = false;
+            return;
+          }
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes);
+          load_a(g, kb, st);
+          ++issued;
+        };
+        const int pre = f.nkb < S ? f.nkb : S;
+        for (int kb = 0; kb < pre; ++kb) issue_w(f, kb);  // fresh stages: no wait
+        griddep_wait();
+        publish(item);
+        for (int kb = pre; ok && kb < f.nkb; ++kb) issue_w(f, kb);
+        while (ok && !*abort_flag) {
+          item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
+          if (item >= ntot) break;
+          f = fdecode(a, item, C::kKB);
+          publish(item);
+          for (int kb = 0; ok && kb < f.nkb; ++kb) issue_w(f, kb);
+        }
+      } else {
+        const int pre = f.nkb < S ? f.nkb : S;
+        for (int kb = 0; kb < pre; ++kb) {
+          mbar_expect_tx(full0 + 8 * kb, C::kABytes);
+          load_a(f, kb, kb);
+        }
+        griddep_wait();
+        publish(item);
+        if (ok && f.stage == 2) ok = wait_stage1(a, f.s, abort_flag);
+        if (ok) {
+          for (int kb = 0; kb < pre; ++kb) {
+            mbar_arrive_expect_tx(full0 + 8 * kb, C::kBBytes);
+            load_b(f, kb, kb);
+          }
+          issued = pre;
+        }
+        for (int kb = pre; ok && kb < f.nkb; ++kb) {
+          const int st = issued % S;
+          if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+            raise(a.err, 23, abort_flag);
             ok = false;
             break;
           }
@@ -356,6 +391,47 @@ __global__ void __launch_bounds__(192, 1)
           load_a(f, kb, st);
           load_b(f, kb, st);
           ++issued;
+        }
+        // then items from the shared counter, in order: stage 1 of every shard, then stage 2
+        while (ok && !*abort_flag) {
+          item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
+          if (item >= ntot) break;
+          f = fdecode(a, item, C::kKB);
+          publish(item);
+          if (!ok) break;
+          int kb = 0;
+          if (f.stage == 2 && ld_acquire(a.sync + kSyncDone + f.s) < (unsigned)(a.rows1 / FBM)) {
+            // weights ahead (their stages were freed by earlier items), then the activations
+            const int la = f.nkb < S ? f.nkb : S;
+            for (; kb < la; ++kb) {
+              const int st = issued % S;
+              if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+                raise(a.err, 24, abort_flag);
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+              load_a(f, kb, st);
+              ++issued;
+            }
+            if (ok) ok = wait_stage1(a, f.s, abort_flag);
+            if (!ok) break;
+            for (int j = 0; j < la; ++j) load_b(f, j, (issued - la + j) % S);
+          } else if (f.stage == 2) {
+            fence_proxy_async_global();
+          }
+          for (; kb < f.nkb; ++kb) {
+            const int st = issued % S;
+            if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+              raise(a.err, 25, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
+            load_a(f, kb, st);
+            load_b(f, kb, st);
+            ++issued;
+          }
         }
       }
       if (ok) publish(-1);
@@ -374,7 +450,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_arrive(iempty0 + 8 * r);
         ++q;
         if (id < 0) break;
-        const FItem f = fdecode(a, id);
+        const FItem f = fdecode(a, id, C::kKB);
         const int acc = it & 1;
         if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) {
           raise(a.err, 27, abort_flag);
@@ -384,18 +460,39 @@ __global__ void __launch_bounds__(192, 1)
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
         bool ok = true;
         for (int kb = 0; kb < f.nkb; ++kb) {
-          const int st = consumed % S;
-          if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1)) {
+          // the activation tile: in the weight stage (bf16), or in its own ring (e4m3)
+          constexpr int NB = FP8 ? C::kSB : S;
+          const int st = consumed % NB;
+          if (!mbar_wait((FP8 ? fullB0 : full0) + 8 * st, (consumed / NB) & 1)) {
             raise(a.err, 28, abort_flag);
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)st * C::kBBytes);
+          const uint32_t bb = smem_u32(sB + (size_t)st * C::kBBytes);
+          if constexpr (FP8) {
+            // the widened weight tile of this k-block waits in tensor-memory slot `slot`
+            const int slot = consumed % C::kASlots;
+            if (!mbar_wait(afull0 + 8 * slot, (consumed / C::kASlots) & 1)) {
+              raise(a.err, 33, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t at = tmem_base + (uint32_t)(C::kACol0 + C::kASlotCols * slot);
 #pragma unroll
-          for (int k = 0; k < FBK / 16; ++k)
-            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
-          mma_commit(empty0 + 8 * st);
+            for (int k = 0; k < C::kKB / 16; ++k)
+              mma_bf16_tmem_a(d, at + 8 * k, sw128_desc(bb + (k / 4) * C::kBSub + 32 * (k % 4)), idesc,
+                              (kb > 0) || k != 0);
+            mma_commit(emptyB0 + 8 * st);
+            mma_commit(aempty0 + 8 * slot);
+          } else {
+            tc_fence_after();
+            const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes);
+#pragma unroll
+            for (int k = 0; k < FBK / 16; ++k)
+              mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+            mma_commit(empty0 + 8 * st);
+          }
           ++consumed;
         }
         if (!ok) break;
@@ -405,6 +502,115 @@ __global__ void __launch_bounds__(192, 1)
       *mma_consumed = consumed;
       mma_commit(drain_bar);
       if (!mbar_wait(drain_bar, 0)) raise(a.err, 29, abort_flag);
+    }
+  } else if (warp == kProducerB) {
+    if constexpr (FP8) {
+      // activation producer (e4m3 weights): follows the item sequence; a stage-2 item first
+      // waits (bounded) for its shard's stage-1 items
+      if (lane == 0) {
+        const uint64_t pol_x = l2_evict_last();
+        griddep_wait();
+        int q = 0;
+        bool ok = true;
+        while (ok) {
+          const int rr = q % kRing;
+          if (!mbar_wait(ifull0 + 8 * rr, (q / kRing) & 1)) {
+            raise(a.err, 36, abort_flag);
+            break;
+          }
+          const int id = ring[rr];
+          mbar_arrive(iempty0 + 8 * rr);
+          ++q;
+          if (id < 0 || *abort_flag) break;
+          const FItem f = fdecode(a, id, C::kKB);
+          if (f.stage == 2 && !wait_stage1(a, f.s, abort_flag)) break;
+          for (int kb = 0; kb < f.nkb; ++kb) {
+            const int st = issuedB % C::kSB;
+            if (!mbar_wait(emptyB0 + 8 * st, ((issuedB / C::kSB) & 1) ^ 1)) {
+              raise(a.err, 37, abort_flag);
+              ok = false;
+              break;
+            }
+            const uint32_t bar = fullB0 + 8 * st;
+            mbar_arrive_expect_tx(bar, C::kBBytes);
+            for (int h = 0; h < C::kKB / FBK; ++h) {
+              const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + h * C::kBSub);
+              if (f.stage == 1)
+                tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
+              else
+                tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
+            }
+            ++issuedB;
+          }
+        }
+      }
+    }
+  } else if (warp >= 6) {
+    if constexpr (FP8) {
+      // converter warps: warp w may address TMEM lanes 32(w%4)..+31, so it widens those rows;
+      // of the two warps of a quarter, warp `sub` takes the 64-wide half `sub` of the stage's
+      // 128-wide k-block.  Each thread takes one row: 64 e4m3 codes (four 16-byte chunks, which
+      // the 128-byte TMA swizzle keeps bank-conflict free: logical chunk c of row r sits at
+      // c ^ (r & 7)), widens them exactly to 32 bf16 pairs and stores them to its TMEM lane,
+      // columns 32 sub .. 32 sub + 31 of the A slot.
+      const int quarter = warp & 3, r = 32 * quarter + lane, sub = (warp - 6) >> 2;
+      const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
+      // software pipeline: a stage's TMEM store completes while the next stage of the same item
+      // is loaded and widened; the store still pending is published (afull) after that.  Never
+      // across items: the next item may wait on stage-1 work that needs this one finished.
+      int pend = -1;
+      auto publish_pending = [&]() {
+        if (pend >= 0) {
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(afull0 + 8 * pend);
+          pend = -1;
+        }
+      };
+      int q = 0, kq = 0;
+      bool ok = true;
+      while (ok) {
+        const int rr = q % kRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(ifull0 + 8 * rr, (q / kRing) & 1))) {
+          raise(a.err, 34, abort_flag);
+          break;
+        }
+        const int id = ring[rr];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(iempty0 + 8 * rr);
+        ++q;
+        if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+        const int nkb = fdecode(a, id, C::kKB).nkb;
+        for (int kb = 0; kb < nkb; ++kb, ++kq) {
+          const int st = kq % S, slot = kq % C::kASlots;
+          if (!__all_sync(0xffffffffu, mbar_wait(full0 + 8 * st, (kq / S) & 1)) ||
+              !__all_sync(0xffffffffu, mbar_wait(aempty0 + 8 * slot, ((kq / C::kASlots) & 1) ^ 1))) {
+            raise(a.err, 35, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint8_t* row = sA + (size_t)st * C::kABytes + r * C::kKB;
+          uint32_t out[32];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * ((4 * sub + j) ^ (r & 7)));
+            const uint2 c0 = e4m3x4_to_bf16x4(v.x), c1 = e4m3x4_to_bf16x4(v.y);
+            const uint2 c2 = e4m3x4_to_bf16x4(v.z), c3 = e4m3x4_to_bf16x4(v.w);
+            out[8 * j + 0] = c0.x; out[8 * j + 1] = c0.y; out[8 * j + 2] = c1.x; out[8 * j + 3] = c1.y;
+            out[8 * j + 4] = c2.x; out[8 * j + 5] = c2.y; out[8 * j + 6] = c3.x; out[8 * j + 7] = c3.y;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(empty0 + 8 * st);  // the weight stage is read: free it
+          publish_pending();
+          tmem_st32(tmem_base + lane_base + (uint32_t)(C::kACol0 + C::kASlotCols * slot + 32 * sub), out);
+          pend = slot;
+          if (kb == nkb - 1) publish_pending();
+        }
+      }
+      publish_pending();
+      if (warp == 6 && lane == 0) *conv_consumed = kq;
     }
   } else {
     // epilogue warps 0..3: global writes only after the grids this one depends on
@@ -422,7 +628,7 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(iempty0 + 8 * rr);
       ++q;
       if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const FItem f = fdecode(a, id);
+      const FItem f = fdecode(a, id, C::kKB);
       const int acc = it & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
         raise(a.err, 31, abort_flag);
@@ -431,11 +637,16 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
       const int p = f.rt * FBM + r;
+      const float wsc = FP8 ? wscale(a, f.stage, f.s, p) : 1.f;  // e4m3: the row's fp32 scale
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(tb + c0, v);
         tmem_ld_wait();
+        if constexpr (FP8) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] *= wsc;
+        }
         if (f.stage == 1) {
           stage1_chunk<KIND>(a, f.s, p, c0, v);
         } else {
@@ -464,7 +675,7 @@ __global__ void __launch_bounds__(192, 1)
           *last_flag = last;
         }
         epi_bar();
-        if (*last_flag) fold_tile(a, f.rt);
+        if (*last_flag) fold_tile<FP8 ? 2 : 4>(a, f.rt);
       }
     }
   }
@@ -472,9 +683,16 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   // drain: wait (bounded) for any TMA copy issued but never consumed
   if (warp == kProducer && lane == 0) {
-    for (int qq = *mma_consumed; qq < issued; ++qq)
+    for (int qq = FP8 ? *conv_consumed : *mma_consumed; qq < issued; ++qq)
       if (!mbar_wait(full0 + 8 * (qq % S), (qq / S) & 1)) {
         atomicExch(a.err, 32u);
+        break;
+      }
+  }
+  if (FP8 && warp == kProducerB && lane == 0) {
+    for (int qq = *mma_consumed; qq < issuedB; ++qq)
+      if (!mbar_wait(fullB0 + 8 * (qq % C::kSB), (qq / C::kSB) & 1)) {
+        atomicExch(a.err, 38u);
         break;
       }
   }
@@ -499,24 +717,30 @@ __global__ void __launch_bounds__(192, 1)
 
 }  // namespace
 
-bool fused_supported(int rows1, int d, int K2, int M, int t) {
+bool fused_supported(int rows1, int d, int K2, int M, int t, bool fp8) {
+  const int kkb = fp8 ? 2 * FBK : FBK;  // e4m3 stages take 128-wide k-blocks
   return M > 0 && M <= kFusedMaxM && t >= 1 && t <= 8 && rows1 % FBM == 0 && rows1 > 0 && d % FBM == 0 &&
-         d > 0 && K2 % FBK == 0 && K2 > 0 && fused_sync_words(d) <= kTcMaxStreamkItems - 64;
+         d > 0 && d % kkb == 0 && K2 % kkb == 0 && K2 > 0 && fused_sync_words(d) <= kTcMaxStreamkItems - 64;
 }
 
-template <int BN, int KIND>
+template <int BN, int KIND, bool FP8>
 static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
-  using C = FCfg<BN>;
+  using C = FCfg<BN, FP8>;
+  // weights: 128-byte box rows in the 128-byte swizzle: bf16 boxes of 64 columns the MMA reads,
+  // or e4m3 boxes of 128 columns the converter warps read
+  const CUtensorMapDataType wty = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle wsw = CU_TENSOR_MAP_SWIZZLE_128B;
+  const cuuint64_t wes = FP8 ? 1 : 2;
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tm[4];
   const cuuint32_t es3[3] = {1, 1, 1}, es2[2] = {1, 1};
   {  // stage-1 weights {K1 = d, rows1, t}
     const cuuint64_t dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.rows1, (cuuint64_t)a.t};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.d * 2, (cuuint64_t)a.stride1};
-    const cuuint32_t box[3] = {FBK, FBM, 1};
-    if (enc(&tm[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w1), dims, strides, box, es3,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t strides[2] = {(cuuint64_t)a.d * wes, (cuuint64_t)a.stride1};
+    const cuuint32_t box[3] = {(cuuint32_t)C::kKB, FBM, 1};
+    if (enc(&tm[0], wty, 3, const_cast<uint8_t*>(a.w1), dims, strides, box, es3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, wsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -531,10 +755,10 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   }
   {  // stage-2 weights {K2, rows2 = d, t}
     const cuuint64_t dims[3] = {(cuuint64_t)a.K2, (cuuint64_t)a.d, (cuuint64_t)a.t};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.K2 * 2, (cuuint64_t)a.stride2};
-    const cuuint32_t box[3] = {FBK, FBM, 1};
-    if (enc(&tm[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint8_t*>(a.w2), dims, strides, box, es3,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K2 * wes, (cuuint64_t)a.stride2};
+    const cuuint32_t box[3] = {(cuuint32_t)C::kKB, FBM, 1};
+    if (enc(&tm[2], wty, 3, const_cast<uint8_t*>(a.w2), dims, strides, box, es3,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, wsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -550,7 +774,7 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(fused_kernel<BN, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(fused_kernel<BN, KIND, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -562,7 +786,7 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   const int grid = ntot < sms ? ntot : sms;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(C::kThreads);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = st;
   // No cooperative launch: it would keep this grid from starting while the previous kernel
@@ -574,25 +798,26 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND>, tm[0], tm[1], tm[2], tm[3], a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND, FP8>, tm[0], tm[1], tm[2], tm[3], a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int KIND>
+template <int KIND, bool FP8>
 static cudaError_t fused_bn(const FusedArgs& a, cudaStream_t st, bool pdl) {
-  if (a.M <= 16) return fused_go<16, KIND>(a, st, pdl);
-  if (a.M <= 32) return fused_go<32, KIND>(a, st, pdl);
-  return fused_go<64, KIND>(a, st, pdl);
+  if (a.M <= 16) return fused_go<16, KIND, FP8>(a, st, pdl);
+  if (a.M <= 32) return fused_go<32, KIND, FP8>(a, st, pdl);
+  return fused_go<64, KIND, FP8>(a, st, pdl);
 }
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
-  if (!fused_supported(a.rows1, a.d, a.K2, a.M, a.t) || !a.err || !a.sync || !a.partials)
+  if (!fused_supported(a.rows1, a.d, a.K2, a.M, a.t, a.fp8 != 0) || !a.err || !a.sync || !a.partials)
     return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.w1) | reinterpret_cast<uintptr_t>(a.w2) | reinterpret_cast<uintptr_t>(a.x) |
        reinterpret_cast<uintptr_t>(a.mid2)) & 15)
     return cudaErrorInvalidValue;
-  return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP>(a, st, pdl) : fused_bn<FUSED_PROJ>(a, st, pdl);
+  if (a.fp8) return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP, true>(a, st, pdl) : fused_bn<FUSED_PROJ, true>(a, st, pdl);
+  return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP, false>(a, st, pdl) : fused_bn<FUSED_PROJ, false>(a, st, pdl);
 }
 
 }  // namespace tpx

@@ -17,12 +17,13 @@ struct FusedArgs {
   int kind;
   int t, M, d;
   // stage 1 (column-parallel): per-shard packed matrix [rows1, K1 = d]
+  int fp8;                       // e4m3 weights: per-row fp32 scales at scales1 / scales2 in each shard
   const uint8_t* w1;
-  uint64_t stride1;
+  uint64_t stride1, scales1;
   int rows1;
   // stage 2 (row-parallel): per-shard packed matrix [rows2 = d, K2]
   const uint8_t* w2;
-  uint64_t stride2;
+  uint64_t stride2, scales2;
   int K2;
   const __nv_bfloat16* x;        // [M, d]
   __nv_bfloat16* mid;            // stage-1 output: h [M, t*rows1/2] or qkv [M, t*rows1]
@@ -39,8 +40,9 @@ constexpr int kFusedMaxM = 64;
 // words of the sync area the fused kernel uses: 128 + one ticket per 128-row output tile
 inline int fused_sync_words(int d) { return 128 + d / 128; }
 
-// Whether the fused kernel supports this block (bf16 weights, 128-row / 64-k tiles, M <= 64).
-bool fused_supported(int rows1, int d, int K2, int M, int t);
+// Whether the fused kernel supports this block (128-row tiles, M <= 64; 64-wide k-blocks for bf16
+// weights, 128-wide for e4m3).
+bool fused_supported(int rows1, int d, int K2, int M, int t, bool fp8);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl);
 
 }  // namespace tpx
