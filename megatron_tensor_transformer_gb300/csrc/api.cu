@@ -100,6 +100,28 @@ uint64_t ticket_bytes(int N) { return align_up((uint64_t)(N / 8 + 1) * 4); }
 // not depend on M, so calls with different M can share one workspace.
 uint64_t sk_bytes() { return align_up(tc_streamk_bytes()); }
 
+// Prefill with e4m3 weights (M > 64): room to widen the largest weight of the shape to bf16
+// once per call; 0 otherwise.  It follows the partials in the workspace.
+uint64_t widen_bytes(const tp_shape* sh, int M) {
+  if (sh->wtype != TP_FP8_E4M3 || M <= kFusedMaxM) return 0;
+  uint64_t b = 0;
+  const uint64_t d = (uint64_t)sh->d;
+  if (sh->ffn > 0) b = 4ull * sh->ffn * d;  // gate + up, 2 bytes each
+  if (sh->n_q_heads > 0 && sh->head_dim > 0) {
+    const uint64_t q = (uint64_t)(sh->n_q_heads + 2 * sh->n_kv_heads) * sh->head_dim * d * 2;
+    if (q > b) b = q;
+  }
+  return align_up(b);
+}
+
+// The widening scratch of a workspace of ws_bytes, or nullptr when it does not fit.
+void* widen_scratch(void* ws, size_t ws_bytes, const tp_shape& sh, int M, uint64_t need) {
+  if (!ws || need == 0) return nullptr;
+  const uint64_t off = sk_bytes() + ticket_bytes(sh.d) + partials_bytes(sh.t, M, sh.d);
+  if (ws_bytes < off + need) return nullptr;
+  return static_cast<uint8_t*>(ws) + off;
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,7 +210,8 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
 size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
   (void)flags;
   if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
-  return (size_t)(sk_bytes() + partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d));
+  return (size_t)(sk_bytes() + partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d) +
+                  widen_bytes(shape, M));
 }
 
 }  // extern "C"
@@ -236,9 +259,39 @@ void set_streamk(TcArgs& a, void* sk_ws) {
                                                (size_t)kTcMaxStreamkItems * 4);
 }
 
+// Weights of a tcgen05 launch.  e4m3 weights stream as they are (widened in shared memory by
+// the kernel), except for prefill-sized M when the workspace has room: then each shard is
+// widened once to bf16 codes in the scratch and the GEMM runs in bf16, with the same per-row
+// scales in its epilogue (same values, same bits).  That GEMM must not start streaming its
+// weights before the widening has finished, so it is launched without programmatic overlap.
+tp_status tc_weights(TcArgs& a, const tp_packed_desc* d, const void* w, int M, void* ws, size_t ws_bytes,
+                     cudaStream_t st, bool& pdl) {
+  const bool fp8 = d->wtype == TP_FP8_E4M3;
+  a.w = static_cast<const uint8_t*>(w);
+  a.shard_stride = d->shard_stride_bytes;
+  a.fp8 = fp8;
+  a.scales_offset = d->scales_offset;
+  if (fp8) {
+    a.scales = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) + d->scales_offset);
+    a.scales_stride = d->shard_stride_bytes / 4;
+  }
+  const uint64_t need = (uint64_t)d->rows_per_shard * d->k_per_shard * 2 * d->shape.t;
+  void* scratch = fp8 ? widen_scratch(ws, ws_bytes, d->shape, M, widen_bytes(&d->shape, M)) : nullptr;
+  if (scratch && need <= widen_bytes(&d->shape, M)) {
+    if (launch_widen_e4m3(static_cast<const uint8_t*>(w), d->shard_stride_bytes, (int)d->rows_per_shard,
+                          (int)d->k_per_shard, d->shape.t, static_cast<bf16*>(scratch), st) != cudaSuccess)
+      return TP_ERR_CUDA;
+    a.w = static_cast<const uint8_t*>(scratch);
+    a.shard_stride = (uint64_t)d->rows_per_shard * d->k_per_shard * 2;
+    a.fp8 = 0;
+    pdl = false;
+  }
+  return TP_OK;
+}
+
 // Column-parallel half over token blocks of at most 64 (skinny) or all tokens (tcgen05).
 tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
-                     int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr) {
+                     int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr, size_t ws_bytes = 0) {
   const int t = d->shape.t;
   const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
@@ -246,10 +299,9 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
   if (pick_tc(flags, rows, K, d->wtype == TP_FP8_E4M3, M)) {
     TcArgs a{};
     a.mode = mode == COLPAR_SWIGLU ? TC_COLPAR_SWIGLU : (mode == COLPAR_F32 ? TC_COLPAR_F32 : TC_COLPAR_BF16);
-    a.w = static_cast<const uint8_t*>(w);
-    a.shard_stride = d->shard_stride_bytes;
-    a.fp8 = d->wtype == TP_FP8_E4M3;
-    a.scales_offset = d->scales_offset;
+    bool pdl = (flags & TP_F_SERIAL) == 0;
+    const tp_status ws_st = tc_weights(a, d, w, M, sk_ws, ws_bytes, st, pdl);
+    if (ws_st != TP_OK) return ws_st;
     a.t = t;
     a.rows = rows;
     a.K = K;
@@ -259,7 +311,7 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     a.out = out;
     a.ldo = ldo;
     set_streamk(a, sk_ws);
-    return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+    return launch_tc(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
   }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
     ColparArgs a{};
@@ -306,10 +358,9 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   }
   if (tc) {
     TcArgs a{};
-    a.w = static_cast<const uint8_t*>(w);
-    a.shard_stride = d->shard_stride_bytes;
-    a.fp8 = d->wtype == TP_FP8_E4M3;
-    a.scales_offset = d->scales_offset;
+    bool pdl = (flags & TP_F_SERIAL) == 0;
+    const tp_status ws_st = tc_weights(a, d, w, M, need_ws ? ws : nullptr, ws_bytes, st, pdl);
+    if (ws_st != TP_OK) return ws_st;
     a.t = t;
     a.rows = N;
     a.K = K;
@@ -330,7 +381,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.y = y;
       a.partials = partials_user;
       a.pM = M;
-      return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+      return launch_tc(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
     }
     for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {  // per-shard partials in the workspace
       const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
@@ -342,7 +393,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.partials = wsP;
       a.pM = mb;
       // unfused: per-shard partials, then the fold kernel
-      if (launch_tc(a, st, (flags & TP_F_SERIAL) == 0) != cudaSuccess) return TP_ERR_CUDA;
+      if (launch_tc(a, st, pdl) != cudaSuccess) return TP_ERR_CUDA;
       if (launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
     }
     return TP_OK;
@@ -460,7 +511,8 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   const int mode = kind == TP_W_GATE_UP ? COLPAR_SWIGLU : (f32 ? COLPAR_F32 : COLPAR_BF16);
   void* sk_ws = nullptr;  // optional stream-K scratch: the head of a tp_workspace_bytes() workspace
   if (ws && aligned16(ws) && ws_bytes >= sk_bytes()) sk_ws = ws;
-  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags, sk_ws);
+  return run_colpar(desc, w, static_cast<const bf16*>(x), M, out, mode, S(stream), flags, sk_ws,
+                    sk_ws ? ws_bytes : 0);
 }
 
 tp_status tp_rowpar_partials(const tp_packed_desc* desc, const void* w, const void* a, int32_t M,
@@ -526,7 +578,7 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu, const void* gu_w, const tp_pa
     return run_fused(FUSED_MLP, gu, gu_w, dn, dn_w, static_cast<const bf16*>(x), static_cast<const bf16*>(residual),
                      M, static_cast<bf16*>(y), static_cast<bf16*>(h_out), static_cast<bf16*>(h_out), ws, flags, s);
   st = run_colpar(gu, gu_w, static_cast<const bf16*>(x), M, h_out, COLPAR_SWIGLU, s, flags,
-                  ws);
+                  ws, ws_bytes);
   if (st != TP_OK) return st;
   return run_rowpar(dn, dn_w, static_cast<const bf16*>(h_out), M, static_cast<const bf16*>(residual),
                     static_cast<bf16*>(y), nullptr, ws, ws_bytes, flags, s);
@@ -555,7 +607,7 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp
     return run_fused(FUSED_PROJ, qkv, qkv_w, o, o_w, static_cast<const bf16*>(x), static_cast<const bf16*>(residual),
                      M, static_cast<bf16*>(y), static_cast<bf16*>(qkv_out), static_cast<bf16*>(o_in), ws, flags, s);
   st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags,
-                  ws);
+                  ws, ws_bytes);
   if (st != TP_OK) return st;
   st = cuda_status(launch_attn1(static_cast<const bf16*>(qkv_out), M, sh.n_q_heads, sh.n_kv_heads,
                                 sh.head_dim, sh.t, static_cast<bf16*>(o_in), s));

@@ -105,6 +105,33 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, fl
 
 // One-token attention per shard: q head h (shard s = h / nq_s) returns the v of its kv group,
 // which lives in the same shard.  qkv is shard-major [q_s | k_s | v_s]; o_in is in head order.
+// Prefill with e4m3 weights: each shard is widened once per call, exactly, to the bf16 codes
+// the tensor cores read (the per-channel scales stay in the GEMM epilogue), so the GEMM runs
+// as a plain bf16 GEMM.  16 codes per thread: one 16-byte streaming load, two 16-byte stores.
+__global__ void widen_e4m3_kernel(const uint8_t* __restrict__ src, uint64_t src_stride, size_t per_shard16,
+                                  int t, __nv_bfloat16* __restrict__ dst) {
+  const size_t n = per_shard16 * (size_t)t;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t s = i / per_shard16, j = i % per_shard16;
+    const uint4 v = ld_stream16(src + s * src_stride + j * 16);
+    const uint2 c0 = e4m3x4_to_bf16x4(v.x), c1 = e4m3x4_to_bf16x4(v.y);
+    const uint2 c2 = e4m3x4_to_bf16x4(v.z), c3 = e4m3x4_to_bf16x4(v.w);
+    uint4* o = reinterpret_cast<uint4*>(dst + i * 16);
+    o[0] = make_uint4(c0.x, c0.y, c1.x, c1.y);
+    o[1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
+  }
+}
+
+cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows, int K, int t, __nv_bfloat16* dst,
+                              cudaStream_t st) {
+  const size_t per_shard16 = (size_t)rows * K / 16;
+  int blocks = (int)std::min<size_t>((per_shard16 * t + 255) / 256, 152 * 16);
+  if (blocks < 1) blocks = 1;
+  widen_e4m3_kernel<<<blocks, 256, 0, st>>>(src, src_stride, per_shard16, t, dst);
+  note_launch();
+  return cudaGetLastError();
+}
+
 __global__ void attn1_kernel(const __nv_bfloat16* __restrict__ qkv, int M, int n_q, int n_kv, int hd,
                              int t, __nv_bfloat16* o_in) {
   const int nqs = n_q / t, nkvs = n_kv / t, group = n_q / n_kv;

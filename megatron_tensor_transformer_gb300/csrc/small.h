@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 namespace tpx {
 
@@ -9,6 +10,10 @@ cudaError_t launch_reduce(const float* P, int t, int M, int d, const __nv_bfloat
                           __nv_bfloat16* y, cudaStream_t st);
 cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, float eps, int M, int d,
                            __nv_bfloat16* out, cudaStream_t st);
+// e4m3 weight shards (shard s at s * src_stride bytes, [rows, K] codes) -> bf16 codes, exactly,
+// in the same per-shard layout, shards packed densely (shard s at s * rows * K elements).
+cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows, int K, int t, __nv_bfloat16* dst,
+                              cudaStream_t st);
 cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
                          __nv_bfloat16* o_in, cudaStream_t st);
 

@@ -136,9 +136,10 @@ __device__ __forceinline__ void raise_error(unsigned code, volatile int* abort_f
   *abort_flag = 1;
 }
 
-// e4m3 weights: the output channel's fp32 scale (row p of shard s); 1 for bf16 weights.
+// e4m3 weights (streamed as e4m3, or widened to bf16 beforehand): the output channel's fp32
+// scale (row p of shard s); 1 for bf16 weights.
 __device__ __forceinline__ float row_scale(const TcArgs& a, int s, int p) {
-  return a.fp8 ? reinterpret_cast<const float*>(a.w + (size_t)s * a.shard_stride + a.scales_offset)[p] : 1.f;
+  return a.scales ? a.scales[(size_t)s * a.scales_stride + p] : 1.f;
 }
 
 // One 16-column chunk of the accumulator for tile row p (of shard s), tokens mf..mf+15.

@@ -20,8 +20,10 @@ struct TcArgs {
   const uint8_t* w;          // packed weights, shard 0
   uint64_t shard_stride;     // bytes
   int t, rows, K;            // shards; per-shard matrix [rows, K]
-  int fp8;                   // e4m3 weights (widened to bf16 in smem; per-row fp32 scales)
+  int fp8;                   // e4m3 weights in `w` (widened to bf16 in smem)
   uint64_t scales_offset;    // FP8: byte offset of the scales inside a shard
+  const float* scales;       // per-row fp32 scales of shard 0 (e4m3 weights), or nullptr
+  uint64_t scales_stride;    // floats from one shard's scales to the next
   const __nv_bfloat16* x;    // activations [M, ldx]
   int ldx, M;
   void* out;                 // colpar output

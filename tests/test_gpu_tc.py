@@ -273,3 +273,21 @@ def test_fp8_widening_is_exact_for_every_code(dev):
     finite = ~np.isnan(want)
     assert np.array_equal(got[finite], want[finite])
     assert np.array_equal(np.signbit(got[finite]), np.signbit(want[finite]))   # -0 stays -0
+
+
+@pytest.mark.parametrize("t,M", [(8, 300), (2, 129)])
+def test_fp8_prefill_widened_once_equals_widened_per_tile(dev, t, M):
+    """Prefill with e4m3 weights: widened once per call into the workspace, then a bf16 GEMM
+    (workspace given), or widened tile by tile in shared memory (no workspace).  Same bf16
+    values, same MMA order, same epilogue scales: the same bits, and the oracle's bar."""
+    m = Mlp(2048, 7168, t, M, dev, seed=15, wtype=tpx.TP_FP8_E4M3)
+    h_once = torch.full((M, m.ffn), float("nan"), dtype=torch.bfloat16, device=dev)
+    h_tile = torch.full_like(h_once, float("nan"))
+    ws = tpx.new_workspace(m.sh, M, dev)
+    assert ws.numel() >= tpx.tp_workspace_bytes(m.sh, M) > tpx.tp_workspace_bytes(m.sh, 64)
+    tpx.tp_colpar_forward(m.gu, m.gu_w, m.x, h_once, flags=TC, ws=ws)
+    tpx.tp_colpar_forward(m.gu, m.gu_w, m.x, h_tile, flags=TC)
+    assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
+    assert torch.equal(h_once.view(torch.int16), h_tile.view(torch.int16))
+    _, h_ref = m.oracle()
+    check_h(bits(h_once), h_ref, what=f"fp8 prefill h t={t} M={M}")
