@@ -114,10 +114,18 @@ uint64_t widen_bytes(const tp_shape* sh, int M) {
   return align_up(b);
 }
 
+// RMSNorm scratch of the fused layer (per-tile sums of squares, two per-token factor arrays);
+// it follows the partials in the workspace.
+uint64_t norm_bytes(int d) { return align_up((uint64_t)fused_norm_words(d) * 4); }
+float* norm_region(void* ws, const tp_shape& sh, int M) {
+  return reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sk_bytes() + ticket_bytes(sh.d) +
+                                  partials_bytes(sh.t, M, sh.d));
+}
+
 // The widening scratch of a workspace of ws_bytes, or nullptr when it does not fit.
 void* widen_scratch(void* ws, size_t ws_bytes, const tp_shape& sh, int M, uint64_t need) {
   if (!ws || need == 0) return nullptr;
-  const uint64_t off = sk_bytes() + ticket_bytes(sh.d) + partials_bytes(sh.t, M, sh.d);
+  const uint64_t off = sk_bytes() + ticket_bytes(sh.d) + partials_bytes(sh.t, M, sh.d) + norm_bytes(sh.d);
   if (ws_bytes < off + need) return nullptr;
   return static_cast<uint8_t*>(ws) + off;
 }
@@ -211,7 +219,7 @@ size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
   (void)flags;
   if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
   return (size_t)(sk_bytes() + partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d) +
-                  widen_bytes(shape, M));
+                  norm_bytes(shape->d) + widen_bytes(shape, M));
 }
 
 }  // extern "C"
@@ -454,7 +462,8 @@ bool pick_fused(uint32_t flags, const tp_packed_desc* d1, const tp_packed_desc* 
 
 tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp_packed_desc* d2, const void* w2,
                     const bf16* x, const bf16* res, int M, bf16* y, bf16* mid, bf16* mid2, void* ws,
-                    uint32_t flags, cudaStream_t st) {
+                    uint32_t flags, cudaStream_t st, float* in_scale = nullptr, int in_norm = 0,
+                    float* out_rms = nullptr, float eps = 0.f) {
   FusedArgs a{};
   a.kind = kind;
   a.t = d1->shape.t;
@@ -479,6 +488,11 @@ tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp
   a.y = y;
   a.partials = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + sk_bytes() + ticket_bytes(a.d));
   a.sync = fused_sync(ws);
+  a.in_scale = in_scale;
+  a.in_norm = in_norm;
+  a.out_rms = out_rms;
+  a.norm_ss = norm_region(ws, d1->shape, M);
+  a.eps = eps;
   a.err = tc_error_word();
   if (!a.err) return TP_ERR_CUDA;
   return launch_fused(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
@@ -647,6 +661,34 @@ tp_status tp_layer_forward(const tp_packed_desc* qkv, const void* qkv_w, const t
   void* b = p;  p += align_up((uint64_t)M * d * 2);
   void* qk = p; p += align_up((uint64_t)M * Q * 2);
   void* h = p;
+  if (pick_fused(flags, qkv, o, M) && pick_fused(flags, gu, dn, M)) {
+    // Decode: two launches.  RMSNorm (gain 1) scales each token by 1/sqrt(mean(x^2) + eps), a
+    // per-token factor, so it multiplies the column-parallel accumulators; the attention
+    // block computes its input's factors itself and, in its fold, those of h1 for the MLP
+    // block (the single-GPU form of the sequence-parallel "reduce-scatter, norm, all-gather").
+    tp_status st = check_desc(qkv, TP_W_QKV, qkv_w);
+    if (st == TP_OK) st = check_desc(o, TP_W_O, o_w);
+    if (st == TP_OK) st = check_desc(gu, TP_W_GATE_UP, gu_w);
+    if (st == TP_OK) st = check_desc(dn, TP_W_DOWN, dn_w);
+    if (st != TP_OK) return st;
+    if (!same_block(qkv->shape, o->shape, false) || !same_block(gu->shape, dn->shape, true))
+      return TP_ERR_LAYOUT_MISMATCH;
+    if ((flags & ~kFwdFlags) || bad_kernel_flags(flags)) return TP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return TP_ERR_ALIGN;
+    if (!ws || ws_bytes < tp_workspace_bytes(&both, M, flags)) return TP_ERR_WORKSPACE;
+    if (!aligned16(ws)) return TP_ERR_ALIGN;
+    float* nb = norm_region(ws, both, M) + kFusedMaxMWords * (d / 128);
+    float* r_x = nb;                    // factors of x (computed by the attention block)
+    float* r_h1 = nb + kFusedMaxMWords;  // factors of h1 (computed by its fold)
+    cudaStream_t s = S(stream);
+    st = run_fused(FUSED_PROJ, qkv, qkv_w, o, o_w, static_cast<const bf16*>(x), static_cast<const bf16*>(x), M,
+                   static_cast<bf16*>(h1), static_cast<bf16*>(qk), static_cast<bf16*>(oi), ws, flags, s, r_x, 1,
+                   r_h1, eps);
+    if (st != TP_OK) return st;
+    return run_fused(FUSED_MLP, gu, gu_w, dn, dn_w, static_cast<const bf16*>(h1), static_cast<const bf16*>(h1), M,
+                     static_cast<bf16*>(y), static_cast<bf16*>(h), static_cast<bf16*>(h), ws, flags, s, r_h1, 0,
+                     nullptr, eps);
+  }
   tp_status st = tp_rmsnorm(x, nullptr, eps, M, (int32_t)d, a, stream);
   if (st != TP_OK) return st;
   st = tp_proj_forward(qkv, qkv_w, o, o_w, a, x, M, h1, qk, oi, ws, ws_bytes, flags, stream);

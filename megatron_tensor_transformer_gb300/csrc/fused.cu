@@ -38,7 +38,7 @@ namespace {
 constexpr int FBM = 128, FBK = 64, kRing = 8;
 constexpr int kProducer = 4, kMma = 5, kProducerB = 14;
 // sync words (all zero between launches)
-constexpr int kSyncItem = 0, kSyncExit = 1, kSyncDone = 8, kSyncTicket = 128;
+constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncDone = 8, kSyncTicket = 128;
 
 // bf16 weights: each stage holds one 64-wide k-block, the 128 x 64 bf16 weight tile (128-byte
 // swizzle) the MMA reads from shared memory.  e4m3 weights: each stage holds a 128-wide k-block,
@@ -218,7 +218,38 @@ __device__ __forceinline__ void fold_tile(const FusedArgs& a, int rt) {
       o.x = (uint32_t)f2bf(acc.x) | ((uint32_t)f2bf(acc.y) << 16);
       o.y = (uint32_t)f2bf(acc.z) | ((uint32_t)f2bf(acc.w) << 16);
       *reinterpret_cast<uint2*>(a.y + base) = o;
+      if (a.out_rms) {
+        // this tile's share of the next block's RMSNorm: sum of squares of the stored bf16
+        // values of token m, four rows per lane, then a fixed shuffle tree over the warp
+        const float e0 = bf16_lo(o.x), e1 = bf16_hi(o.x), e2 = bf16_lo(o.y), e3 = bf16_hi(o.y);
+        float ss = ((e0 * e0 + e1 * e1) + e2 * e2) + e3 * e3;
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+        if ((threadIdx.x & 31) == 0) a.norm_ss[(size_t)m * (a.d / FBM) + rt] = ss;
+      }
     }
+  }
+}
+
+// Per-token RMSNorm factor of x [M, d] (gain 1): 1/sqrt(mean(x^2) + eps), by the 128 epilogue
+// threads, one warp per token, each lane eight values per step, then a fixed shuffle tree.
+__device__ __forceinline__ void input_norm(const FusedArgs& a) {
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  for (int m = w; m < a.M; m += 4) {
+    float ss = 0.f;
+    for (int k = 8 * l; k < a.d; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.d + k);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float e0 = bf16_lo(u[j]), e1 = bf16_hi(u[j]);
+        ss += e0 * e0;
+        ss += e1 * e1;
+      }
+    }
+#pragma unroll
+    for (int sh = 16; sh > 0; sh >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, sh);
+    if (l == 0) a.in_scale[m] = 1.f / sqrtf(ss / (float)a.d + a.eps);
   }
 }
 
@@ -241,6 +272,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 2);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
   int* conv_consumed = reinterpret_cast<int*>(tmem_slot + 4);  // e4m3: weight stages the converters took
+  volatile int* norm_last = reinterpret_cast<volatile int*>(tmem_slot + 5);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
                  tempty0 = smem_u32(bars + 2 * S + 2), ifull0 = smem_u32(bars + 2 * S + 4),
                  iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing),
@@ -616,6 +648,13 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
     // epilogue warps 0..3: global writes only after the grids this one depends on
     griddep_wait();
     const int r = warp * 32 + lane;  // row inside the 128-row tile
+    if (a.in_norm && blockIdx.x == 0) {  // the input's RMSNorm factors, published to every CTA
+      input_norm(a);
+      __threadfence();
+      epi_bar();
+      if (threadIdx.x == 0) red_release_add(a.sync + kSyncInNorm, 1u);
+    }
+    bool scale_ready = a.in_norm == 0;
     int q = 0, it = 0;
     while (true) {
       const int rr = q % kRing;
@@ -638,6 +677,18 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
       const int p = f.rt * FBM + r;
       const float wsc = FP8 ? wscale(a, f.stage, f.s, p) : 1.f;  // e4m3: the row's fp32 scale
+      const bool tok_scale = f.stage == 1 && a.in_scale != nullptr;
+      if (tok_scale && !scale_ready) {  // wait (bounded) for CTA 0's input norm
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire(a.sync + kSyncInNorm) == 0u) {
+          if (globaltimer_ns() - t0 > 2000000000ull) {
+            raise(a.err, 39, abort_flag);
+            break;
+          }
+          __nanosleep(64);
+        }
+        scale_ready = true;
+      }
 #pragma unroll 1
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
@@ -646,6 +697,10 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
         if constexpr (FP8) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] *= wsc;
+        }
+        if (tok_scale) {  // RMSNorm of the input as a per-token factor on the accumulator
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] *= __ldcg(a.in_scale + c0 + j);
         }
         if (f.stage == 1) {
           stage1_chunk<KIND>(a, f.s, p, c0, v);
@@ -675,7 +730,29 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
           *last_flag = last;
         }
         epi_bar();
-        if (*last_flag) fold_tile<FP8 ? 2 : 4>(a, f.rt);
+        if (*last_flag) {
+          fold_tile<FP8 ? 2 : 3>(a, f.rt);
+          if (a.out_rms) {
+            // the tile whose fold comes last sums every tile's share, in tile order
+            __threadfence();
+            epi_bar();
+            if (threadIdx.x == 0) {
+              const int nt = a.d / FBM;
+              const unsigned old = atomicAdd(a.sync + kSyncNormTiles, 1u);
+              const int lastn = old == (unsigned)(nt - 1);
+              if (lastn) a.sync[kSyncNormTiles] = 0u;
+              __threadfence();
+              *norm_last = lastn;
+            }
+            epi_bar();
+            if (*norm_last && threadIdx.x < a.M) {
+              const int nt = a.d / FBM;
+              float ss = 0.f;
+              for (int t2 = 0; t2 < nt; ++t2) ss += __ldcg(a.norm_ss + (size_t)threadIdx.x * nt + t2);
+              a.out_rms[threadIdx.x] = 1.f / sqrtf(ss / (float)a.d + a.eps);
+            }
+          }
+        }
       }
     }
   }
@@ -706,9 +783,12 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
     __threadfence();
     if (atomicAdd(a.sync + kSyncExit, 1u) == gridDim.x - 1) {
       a.sync[kSyncItem] = 0u;
+      a.sync[kSyncInNorm] = 0u;
       for (int s = 0; s < 8; ++s) a.sync[kSyncDone + s] = 0u;
-      if (*reinterpret_cast<volatile unsigned*>(a.err) != 0u)
+      if (*reinterpret_cast<volatile unsigned*>(a.err) != 0u) {
         for (int rt = 0; rt < a.d / FBM; ++rt) a.sync[kSyncTicket + rt] = 0u;
+        a.sync[kSyncNormTiles] = 0u;
+      }
       a.sync[kSyncExit] = 0u;
       __threadfence();
     }

@@ -34,9 +34,22 @@ struct FusedArgs {
   float* partials;               // [t][M][d] fp32
   unsigned* sync;                // zeroed words: item counter, exit counter, per-shard counts, tile tickets
   unsigned* err;                 // device error word (fail fast, and set when a bounded wait gives up)
+  // RMSNorm (gain 1) folded into the block.  Normalising the input is a per-token factor, so it
+  // multiplies the column-parallel accumulators: in_scale[m] (nullable, 64 floats).  With
+  // in_norm the kernel first computes in_scale[m] = 1/sqrt(mean_k x[m][k]^2 + eps) from x.
+  // out_rms (nullable, 64 floats): the fold also yields the same factor of the block's bf16
+  // output y, for the next block; norm_ss: scratch of 64 x d/128 fp32.
+  float* in_scale;
+  int in_norm;
+  float* out_rms;
+  float* norm_ss;
+  float eps;
 };
 
 constexpr int kFusedMaxM = 64;
+constexpr int kFusedMaxMWords = 64;  // per-token arrays are sized for kFusedMaxM tokens
+// fp32 words of RMSNorm scratch a fused block with a folded norm needs: norm_ss, in_scale, out_rms
+inline int fused_norm_words(int d) { return kFusedMaxMWords * (d / 128) + 2 * kFusedMaxMWords; }
 // words of the sync area the fused kernel uses: 128 + one ticket per 128-row output tile
 inline int fused_sync_words(int d) { return 128 + d / 128; }
 

@@ -123,3 +123,45 @@ def test_405b_layer_full_size_sampled_tokens(dev):
     lay.check_blocks(bits(x), scratch, ws, what="405B layer, 2 tokens")
     y = lay.gpu(x, scratch, ws)
     check_layer(bits(y), lay.oracle(bits(x)), what="405B layer, 2 tokens")
+
+
+@pytest.mark.parametrize("M,wtype", [(16, tpx.TP_BF16), (5, tpx.TP_BF16), (16, tpx.TP_FP8_E4M3)])
+def test_layer_norm_folded_into_blocks(dev, M, wtype):
+    """Decode layers run as two launches: the RMSNorms become per-token factors on the
+    column-parallel accumulators (the attention block computes its input's factors, and its
+    fold those of h1).  Against the oracle, against the path with separate RMSNorm launches
+    (no bf16 rounding of the normalised input here, so the two differ by rounding only), and
+    bit for bit from run to run."""
+    # e4m3 weights stream in 128-wide k-blocks: the down projection's K per shard (ffn / t) must
+    # be a multiple of 128 for the one-launch block
+    d, ffn, n_q, n_kv, hd, t = 2048, 6656 if wtype == tpx.TP_BF16 else 7168, 16, 8, 128, 8
+    lay = Layer(d, ffn, n_q, n_kv, hd, t, 0, dev, seed=4)
+    if wtype != tpx.TP_BF16:
+        lay.sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=wtype)
+        lay.q_w, lay.q = tpx.tp_partition_weights(lay.sh, tpx.TP_W_QKV, lay.wqkv)
+        lay.o_w, lay.o = tpx.tp_partition_weights(lay.sh, tpx.TP_W_O, lay.wo)
+        lay.gu_w, lay.gu = tpx.tp_partition_weights(lay.sh, tpx.TP_W_GATE_UP, lay.wg, lay.wu)
+        lay.dn_w, lay.dn = tpx.tp_partition_weights(lay.sh, tpx.TP_W_DOWN, lay.wd)
+    scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
+    ws = tpx.new_workspace(lay.sh, M, dev)
+    x = inputs.normal_bf16((M, d), 1.0, 4, inputs.STREAM_X, dev)
+    n0 = tpx.tp_launch_count()
+    y = lay.gpu(x, scratch, ws)
+    assert tpx.tp_launch_count() - n0 == 2
+    y_split = torch.full_like(x, float("nan"))
+    tpx.tp_layer_forward(lay.q, lay.q_w, lay.o, lay.o_w, lay.gu, lay.gu_w, lay.dn, lay.dn_w, x, y_split,
+                         scratch, ws, flags=tpx.TP_F_SPLIT_BLOCK)
+    assert tpx.tp_sync(timeout_ms=30000) == tpx.TP_OK
+    if wtype == tpx.TP_BF16:
+        check_layer(bits(y), lay.oracle(bits(x)), what=f"folded-norm layer M={M}")
+    else:
+        deq = []
+        for w in (lay.wqkv, lay.wo, lay.wg, lay.wu, lay.wd):
+            q, s = O.quantize_fp8_per_channel(O.as_f64(bits(w)))
+            deq.append(O.dequantize_fp8(q, s))
+        y_ref, _ = O.layer(bits(x), *deq, n_q, n_kv, hd)
+        check_layer(bits(y), y_ref, what=f"folded-norm fp8 layer M={M}")
+    check_layer(bits(y), O.as_f64(bits(y_split)), what="folded vs separate norms")
+    for _ in range(2):
+        y2 = lay.gpu(x, scratch, ws)
+        assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
