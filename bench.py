@@ -344,10 +344,12 @@ def run_layer(args, rank, world, local):
     h = torch.empty((M, ffn), dtype=torch.bfloat16, device=dev)
     ws = tpx.new_workspace(sh, M, dev)
     K = args.steps
+    kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY,
+          "split": tpx.TP_F_SPLIT_BLOCK}[args.kernel]
 
     def step():
-        tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y1, qkv, o_in, ws, stream=stream)
-        tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, stream=stream)
+        tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y1, qkv, o_in, ws, flags=kf, stream=stream)
+        tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, flags=kf, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -368,9 +370,9 @@ def run_layer(args, rank, world, local):
         c0.record(stream)
         for _ in range(K):
             if prefill:
-                tpx.tp_colpar_forward(gu, gu_w, y1, h, stream=stream, ws=ws)
+                tpx.tp_colpar_forward(gu, gu_w, y1, h, flags=kf & ~tpx.TP_F_SPLIT_BLOCK, stream=stream, ws=ws)
             else:
-                tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, stream=stream)
+                tpx.tp_mlp_forward(gu, gu_w, dn, dn_w, y1, y1, y, h, ws, flags=kf, stream=stream)
         c1.record(stream)
         c1.synchronize()
     ms = a.elapsed_time(b) / K
@@ -386,7 +388,7 @@ def run_layer(args, rank, world, local):
     out = {"metric": METRIC, "workload": args.workload, "n_gpus": 1, "steps": K, "warmup": args.warmup,
            "ms_per_step": ms, "dtype": "e4m3 weights, bf16 math" if fp8 else "bf16", "data": "synthetic",
            "config": {"workload": args.workload, "d": d, "ffn": ffn, "n_q": n_q, "n_kv": n_kv,
-                      "head_dim": hd, "t": t, "M": M},
+                      "head_dim": hd, "t": t, "M": M, "kernel": args.kernel},
            "gpu_launches": launches, "clocks": clk.summary()}
     if prefill:
         out.update({"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "higher_is_better": True,

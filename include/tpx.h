@@ -103,8 +103,9 @@ typedef struct {
                                      flight on the stream (tp_partition_weights returns with them
                                      complete).  Activations are always read after earlier work ends. */
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
-#define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernel (bf16 weights, rows % 128, K % 64);
-                                     default: tcgen05 where supported, else mma.sync */
+#define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernels (rows % 128, K % 64); default:
+                                     tcgen05 where supported, except e4m3 weights at decode token counts
+                                     (M <= 64), which stream faster through the mma.sync kernel */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, bf16 weights, 128-row
                                      and 64-k tiles) runs as ONE persistent launch: the column-parallel

@@ -19,7 +19,7 @@ from oracle import tp_oracle as O
 from tests.test_gpu_parity import Mlp, bits, check_close, check_h, run_proj
 
 pytestmark = pytest.mark.gpu
-UNF, SPLIT = tpx.TP_F_UNFUSED_REDUCE, tpx.TP_F_SPLIT_BLOCK
+UNF, SPLIT, TC = tpx.TP_F_UNFUSED_REDUCE, tpx.TP_F_SPLIT_BLOCK, tpx.TP_F_KERNEL_TC
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -171,15 +171,15 @@ def test_fused_fp8_mlp_bits_equal_split_partials_path(dev, M):
     shared memory.  Both feed the same bf16 values to the same MMA sequence and scale in the
     epilogue, so at the 8B shape (no split items on either path) the bits agree."""
     m = Mlp(4096, 14336, 8, M, dev, seed=12, wtype=FP8)
-    yf, hf = m.run()
-    yu, hu = m.run(flags=UNF)
+    yf, hf = m.run(flags=TC)
+    yu, hu = m.run(flags=TC | UNF)
     assert same_bits(hf, hu), "h differs"
     assert same_bits(yf, yu), "y differs"
-    y2, _ = m.run()
+    y2, _ = m.run(flags=TC)
     assert same_bits(yf, y2)
 
 
-def _fp8_proj(d, n_q, n_kv, hd, t, M, dev, seed):
+def _fp8_proj(d, n_q, n_kv, hd, t, M, dev, seed, flags=0):
     x, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, M, seed=seed, device=dev)
     sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=FP8)
     q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv)
@@ -189,7 +189,7 @@ def _fp8_proj(d, n_q, n_kv, hd, t, M, dev, seed):
     qkv = torch.full((M, Q), float("nan"), dtype=torch.bfloat16, device=dev)
     o_in = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = tpx.new_workspace(sh, M, dev)
-    tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y, qkv, o_in, ws)
+    tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y, qkv, o_in, ws, flags)
     assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
     deq = []
     for w in (wqkv, wo):
@@ -200,18 +200,20 @@ def _fp8_proj(d, n_q, n_kv, hd, t, M, dev, seed):
     return qkv, qkv_ref[:, cols], y, y_ref
 
 
+@pytest.mark.parametrize("flags", [TC, 0], ids=["tcgen05-fused", "default"])
 @pytest.mark.parametrize("t,M", [(1, 16), (2, 5), (4, 64), (8, 16)])
-def test_fused_fp8_blocks_vs_oracle(dev, t, M):
+def test_fused_fp8_blocks_vs_oracle(dev, t, M, flags):
     """Against the oracle on the dequantised weights; the bf16 bar (stricter than the 3e-2 FP8
-    bar) holds for both blocks."""
+    bar) holds for both blocks, on the fused tcgen05 path and on the default e4m3 decode path
+    (the mma.sync kernel)."""
     m = Mlp(2048, 7168, t, M, dev, seed=13, wtype=FP8)
-    y, h = m.run()
+    y, h = m.run(flags=flags)
     y_ref, h_ref = m.oracle()
-    check_close(bits(y), y_ref, what=f"fused fp8 MLP t={t} M={M}")
-    check_h(bits(h), h_ref, what=f"fused fp8 h t={t} M={M}")
-    y0, _ = m.run(residual=False)
+    check_close(bits(y), y_ref, what=f"fp8 MLP t={t} M={M} flags={flags}")
+    check_h(bits(h), h_ref, what=f"fp8 h t={t} M={M}")
+    y0, _ = m.run(residual=False, flags=flags)
     y0_ref, _ = m.oracle(residual=False)
-    check_close(bits(y0), y0_ref, what=f"fused fp8 MLP no residual t={t} M={M}")
-    qkv, qkv_ref, y, y_ref = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=14)
+    check_close(bits(y0), y0_ref, what=f"fp8 MLP no residual t={t} M={M}")
+    qkv, qkv_ref, y, y_ref = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=14, flags=flags)
     check_close(bits(qkv), qkv_ref, what=f"fused fp8 qkv t={t} M={M}")
     check_close(bits(y), y_ref, what=f"fused fp8 o_proj t={t} M={M}")

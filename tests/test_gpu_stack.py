@@ -50,10 +50,10 @@ class Layer:
         self.dn_w, self.dn = tpx.tp_partition_weights(self.sh, tpx.TP_W_DOWN, self.wd)
         self.heads = (n_q, n_kv, hd)
 
-    def gpu(self, x, scratch, ws):
+    def gpu(self, x, scratch, ws, flags=0):
         y = torch.full_like(x, float("nan"))
         tpx.tp_layer_forward(self.q, self.q_w, self.o, self.o_w, self.gu, self.gu_w, self.dn, self.dn_w,
-                             x, y, scratch, ws)
+                             x, y, scratch, ws, flags=flags)
         assert tpx.tp_sync(timeout_ms=30000) == tpx.TP_OK
         return y
 
@@ -145,8 +145,9 @@ def test_layer_norm_folded_into_blocks(dev, M, wtype):
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, d), 1.0, 4, inputs.STREAM_X, dev)
+    fl = 0 if wtype == tpx.TP_BF16 else tpx.TP_F_KERNEL_TC  # e4m3 decode is fused only when asked
     n0 = tpx.tp_launch_count()
-    y = lay.gpu(x, scratch, ws)
+    y = lay.gpu(x, scratch, ws, fl)
     assert tpx.tp_launch_count() - n0 == 2
     y_split = torch.full_like(x, float("nan"))
     tpx.tp_layer_forward(lay.q, lay.q_w, lay.o, lay.o_w, lay.gu, lay.gu_w, lay.dn, lay.dn_w, x, y_split,
@@ -163,5 +164,5 @@ def test_layer_norm_folded_into_blocks(dev, M, wtype):
         check_layer(bits(y), y_ref, what=f"folded-norm fp8 layer M={M}")
     check_layer(bits(y), O.as_f64(bits(y_split)), what="folded vs separate norms")
     for _ in range(2):
-        y2 = lay.gpu(x, scratch, ws)
+        y2 = lay.gpu(x, scratch, ws, fl)
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
