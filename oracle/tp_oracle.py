@@ -282,6 +282,101 @@ def pack_colpar(w_list, kind, t, **shape):
     return out
 
 
+# --------------------------------------------------------------------------
+# vocabulary-parallel edges of the model: the lm_head is column-parallel over the
+# vocabulary (each shard's logits are a slice of the output, so the "all-gather" is a
+# concatenation) and the embedding table is split by vocabulary rows (each shard holds
+# the rows of its own id range; a lookup is the sum over shards of "my row, or zeros",
+# scalablesystem.dev "The Tensor-Parallel Shard Group", vocab shard).  The vocabulary is
+# padded with zero rows to a multiple of 128 per shard.
+# --------------------------------------------------------------------------
+
+VOCAB_ALIGN = 128
+
+
+def vocab_padded(V, t):
+    """V rounded up so that every one of the t shards holds a multiple of 128 ids."""
+    q = VOCAB_ALIGN * t
+    return (V + q - 1) // q * q
+
+
+def vocab_columns(s, t, V):
+    """Vocabulary ids (output columns of the lm_head) of shard s's packed rows; ids >= V are
+    padding."""
+    vs = vocab_padded(V, t) // t
+    return s * vs + np.arange(vs)
+
+
+def pack_vocab(w, t):
+    """lm_head W [d, V] -> t shards [Vs, d]: row r of shard s = column s*Vs + r of W, zero for
+    padding ids."""
+    w = np.asarray(w)
+    d, V = w.shape
+    out = []
+    for s in range(t):
+        ids = vocab_columns(s, t, V)
+        shard = np.zeros((len(ids), d), dtype=w.dtype)
+        ok = ids < V
+        shard[ok] = w[:, ids[ok]].T
+        out.append(shard)
+    return out
+
+
+def pack_embed(e, t):
+    """Embedding table E [V, d] -> t shards [Vs, d]: row r of shard s = E[s*Vs + r], zero for
+    padding ids."""
+    e = np.asarray(e)
+    V, d = e.shape
+    out = []
+    for s in range(t):
+        ids = vocab_columns(s, t, V)
+        shard = np.zeros((len(ids), d), dtype=e.dtype)
+        ok = ids < V
+        shard[ok] = e[ids[ok]]
+        out.append(shard)
+    return out
+
+
+def lm_head(x, w):
+    """logits = x W for W [d, V]: the plain product, unsharded."""
+    return as_f64(x) @ as_f64(w)
+
+
+def lm_head_sharded(x, w, t):
+    """The same logits evaluated shard by shard from pack_vocab's shards and concatenated in
+    shard order (the column-parallel output needs no reduction), cut to the V real ids."""
+    x = as_f64(x)
+    V = np.asarray(w).shape[1]
+    parts = [x @ as_f64(sh).T for sh in pack_vocab(w, t)]
+    return np.concatenate(parts, axis=1)[:, :V]
+
+
+def embed_lookup(ids, e):
+    """x[m] = E[ids[m]]; an id outside [0, V) gives a zero row (no shard owns it)."""
+    e = as_f64(e)
+    ids = np.asarray(ids, dtype=np.int64)
+    out = np.zeros((len(ids), e.shape[1]))
+    ok = (ids >= 0) & (ids < e.shape[0])
+    out[ok] = e[ids[ok]]
+    return out
+
+
+def embed_lookup_sharded(ids, e, t):
+    """The vocabulary-parallel form: every shard contributes its row if the id is in its range,
+    else zeros, and the contributions are summed in shard order."""
+    V = np.asarray(e).shape[0]
+    vs = vocab_padded(V, t) // t
+    ids = np.asarray(ids, dtype=np.int64)
+    acc = np.zeros((len(ids), np.asarray(e).shape[1]))
+    for s, sh in enumerate(pack_embed(e, t)):
+        local = ids - s * vs
+        mine = (local >= 0) & (local < vs) & (ids < V)
+        part = np.zeros_like(acc)
+        part[mine] = as_f64(sh)[local[mine]]
+        acc = acc + part
+    return acc
+
+
 def pack_rowpar(w, t):
     """Row-parallel shards of W [in,out]: shard s = [out, in/t], element [n,k] = W[s*in/t + k, n]."""
     w = np.asarray(w)

@@ -315,3 +315,53 @@ def test_layer_reduces_to_its_blocks():
     m, _ = O.mlp(O.rmsnorm(p), wg, wu, wd, residual=p)
     assert np.allclose(y, m, rtol=1e-13, atol=1e-13)
 
+
+
+# ---------------------------------------------------------------- vocabulary-parallel edges
+
+def test_vocab_padding_matches_the_shard_alignment():
+    # Llama 3's 128256 ids over 8 shards: 16032 each is not a multiple of 128, so each shard
+    # is padded to 16128 (126 x 128); with t = 1 the 128256 ids need 1002 x 128 = 128256
+    assert O.vocab_padded(128256, 8) == 129024 and O.vocab_padded(128256, 8) // 8 == 16128
+    assert O.vocab_padded(128256, 1) == 128256
+    assert O.vocab_padded(1000, 4) == 1024 and O.vocab_padded(1024, 8) == 1024
+
+
+@pytest.mark.parametrize("t", [1, 2, 4, 8])
+def test_lm_head_sharded_concatenation_equals_unsharded(t):
+    rng = np.random.default_rng(t)
+    d, V, M = 24, 1000, 3            # 1000 ids: the last shard carries padding
+    x = rng.integers(-3, 4, size=(M, d)).astype(np.float64)
+    w = rng.integers(-3, 4, size=(d, V)).astype(np.float64)
+    np.testing.assert_array_equal(O.lm_head_sharded(x, w, t), O.lm_head(x, w))
+
+
+def test_lm_head_brute_force_and_pack_layout():
+    rng = np.random.default_rng(7)
+    d, V, M, t = 5, 300, 2, 2
+    x = rng.normal(size=(M, d))
+    w = rng.normal(size=(d, V))
+    ref = np.array([[sum(x[m, k] * w[k, v] for k in range(d)) for v in range(V)] for m in range(M)])
+    np.testing.assert_allclose(O.lm_head(x, w), ref, rtol=1e-12, atol=1e-12)
+    shards = O.pack_vocab(w, t)       # Vp = 512: 256 ids per shard, ids 300..511 padding
+    assert [sh.shape for sh in shards] == [(256, d), (256, d)]
+    np.testing.assert_array_equal(shards[0][7], w[:, 7])
+    np.testing.assert_array_equal(shards[1][0], w[:, 256])
+    np.testing.assert_array_equal(shards[1][43], w[:, 299])
+    assert not shards[1][44:].any()
+
+
+def test_embedding_lookup_by_hand_and_vocab_parallel_sum():
+    V, d, t = 10, 3, 2                # Vp = 256: shard 0 owns ids 0..127, shard 1 only padding
+    e = np.arange(V * d, dtype=np.float64).reshape(V, d)
+    ids = [3, 0, 9, 12, -1]
+    got = O.embed_lookup(ids, e)
+    np.testing.assert_array_equal(got[0], [9, 10, 11])
+    np.testing.assert_array_equal(got[1], [0, 1, 2])
+    np.testing.assert_array_equal(got[2], [27, 28, 29])
+    assert not got[3].any() and not got[4].any()          # ids no shard owns: zero rows
+    for tt in (1, 2, 4, 8):
+        np.testing.assert_array_equal(O.embed_lookup_sharded(ids, e, tt), got)
+    shards = O.pack_embed(e, 2)
+    np.testing.assert_array_equal(shards[0][:V], e)
+    assert not shards[0][V:].any() and not shards[1].any()
