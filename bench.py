@@ -473,6 +473,72 @@ def run_stack(args, rank, world, local):
         "gpu_launches": launches, "clocks": clk.summary()}), flush=True)
 
 
+def run_lm_head(args, rank, world, local):
+    """Llama-3 70B output layer: the vocabulary-parallel lm_head (d 8192, 128256 ids over t=8
+    shards, padded to 16128 per shard), decode M=32, fp32 logits, through tp_lm_head_forward;
+    plus the vocabulary-parallel embedding lookup of the same tokens."""
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+
+    d, V, t, M = 8192, 128256, args.t or 8, 32
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = tpx.make_shape(d, t=t, vocab=V)
+    w = inputs.normal_bf16((d, V), 0.02, 0, 70, dev)
+    w_p, wd = tpx.tp_partition_weights(sh, tpx.TP_W_VOCAB, w, stream=stream)
+    del w
+    e = inputs.normal_bf16((V, d), 1.0, 0, 71, dev)
+    e_p, ed = tpx.tp_partition_weights(sh, tpx.TP_W_EMBED, e, stream=stream)
+    del e
+    torch.cuda.empty_cache()
+    ids = torch.randint(0, V, (M,), generator=torch.Generator(device=dev).manual_seed(0), device=dev,
+                        dtype=torch.int32)
+    x = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((M, V), dtype=torch.float32, device=dev)
+    ws = tpx.new_workspace(sh, M, dev)
+    K = args.steps
+
+    def step():
+        tpx.tp_embed_lookup(ed, e_p, ids, x, stream=stream)
+        tpx.tp_lm_head_forward(wd, w_p, x, logits, ws=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = tpx.tp_launch_count()
+        with Clocks(f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
+            a.record(stream)
+            for _ in range(K):
+                step()
+            b.record(stream)
+            b.synchronize()
+        launches = tpx.tp_launch_count() - n0
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            tpx.tp_lm_head_forward(wd, w_p, x, logits, ws=ws, stream=stream)
+        c1.record(stream)
+        c1.synchronize()
+    ms, head_ms = a.elapsed_time(b) / K, c0.elapsed_time(c1) / K
+    wbytes = 2.0 * d * V                         # the lm_head weights, read once
+    head_bytes = wbytes + 2.0 * M * d + 4.0 * M * V
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    print(json.dumps({
+        "metric": METRIC, "workload": "70b-lm-head-decode", "value": M / (ms * 1e-3), "unit": "tokens/s",
+        "higher_is_better": True, "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "70b-lm-head-decode", "d": d, "vocab": V, "t": t, "M": M},
+        "hbm_gbs_step": wbytes / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "tc_kernel (vocabulary-parallel lm_head)",
+                     "achieved": head_bytes / (head_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": head_bytes / (head_ms * 1e-3) / 1e9 / pk["hbm_gbs"]},
+        "gpu_launches": launches, "clocks": clk.summary()}), flush=True)
+
+
 def run_e2e(args, gu, gu_w, dn, dn_w, sh, dev):
     """Through the public C-ABI call tp_mlp_forward with HOST buffers: every step copies each
     batch's x from pinned host memory, runs the block, and copies y back."""
@@ -517,7 +583,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="8b-mlp-decode",
-                    choices=["8b-mlp-decode", "405b-stack-decode"] + sorted(LAYERS),
+                    choices=["8b-mlp-decode", "405b-stack-decode", "70b-lm-head-decode"] + sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny", "split"],
@@ -529,6 +595,8 @@ def main():
     rank, world, local = dist_setup()
     if args.workload == "405b-stack-decode":
         run_stack(args, rank, world, local)
+    elif args.workload == "70b-lm-head-decode":
+        run_lm_head(args, rank, world, local)
     elif args.workload != "8b-mlp-decode":
         run_layer(args, rank, world, local)
     elif args.impl == "reference":

@@ -55,15 +55,20 @@ typedef enum {
   TP_W_GATE_UP = 0, /* column-parallel W_gate and W_up, [d, ffn] each */
   TP_W_DOWN = 1,    /* row-parallel W_down, [ffn, d] */
   TP_W_QKV = 2,     /* column-parallel W_qkv, [d, (n_q + 2 n_kv) * head_dim] */
-  TP_W_O = 3        /* row-parallel W_o, [n_q * head_dim, d] */
+  TP_W_O = 3,       /* row-parallel W_o, [n_q * head_dim, d] */
+  TP_W_VOCAB = 4,   /* lm_head W, [d, vocab], column-parallel over the vocabulary (bf16 only) */
+  TP_W_EMBED = 5    /* embedding table E, [vocab, d], split by vocabulary rows (bf16 only) */
 } tp_wkind;
 
 /* Model dims and the shard count.  ffn is used by GATE_UP/DOWN, the head dims by
- * QKV/O.  t must be 1, 2, 4 or 8 and divide ffn, n_q and n_kv ("TP degree must
- * divide the KV heads"; t > n_kv head replication is not supported). */
+ * QKV/O, vocab by VOCAB/EMBED.  t must be 1, 2, 4 or 8 and divide ffn, n_q and n_kv ("TP
+ * degree must divide the KV heads"; t > n_kv head replication is not supported).  The
+ * vocabulary is padded with zero rows so that each shard holds a multiple of 128 ids:
+ * vocab_padded = round_up(vocab, 128 t), V_s = vocab_padded / t ids per shard. */
 typedef struct {
   int32_t d, ffn, n_q_heads, n_kv_heads, head_dim, t;
   int32_t wtype; /* tp_wtype */
+  int32_t vocab;
 } tp_shape;
 
 #define TP_DESC_MAGIC 0x54505831u /* "TPX1" */
@@ -82,6 +87,10 @@ typedef struct {
  *            q head h uses kv head h / (n_q/n_kv), so a GQA group never straddles shards.
  *   DOWN/O:  shard s holds rows [s*K_s, (s+1)*K_s) of the [in, out] weight,
  *            transposed: element [n][k] = W[s*K_s + k][n]; FP8 scales replicated.
+ *   VOCAB:   shard s holds vocabulary ids [s*V_s, (s+1)*V_s): row r = column s*V_s + r of
+ *            the [d, vocab] lm_head weight, zero for padding ids (>= vocab).
+ *   EMBED:   shard s holds rows [s*V_s, (s+1)*V_s) of the [vocab, d] table as they are,
+ *            zero for padding ids.
  * FP8: s_n = absmax over the whole unsharded input dim of column n / 448 (fp32),
  * 1 for an all-zero column; code = e4m3 RNE satfinite(W / s_n) (fp32 divide). */
 typedef struct {
@@ -217,6 +226,21 @@ tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc /* host */, const
 
 /* Bytes of the static scratch array tp_rowpar_forward_noalloc uses. */
 size_t tp_noalloc_scratch_capacity(void);
+
+/* Vocabulary-parallel lm_head (the column-parallel GEMM at the model's output edge; each shard's
+ * logits are a slice of the output, so the pages' all-gather is a concatenation, scalablesystem.dev
+ * "The Tensor-Parallel Shard Group"): logits[m][v] = sum_k x[m][k] W[k][v] for v < vocab, fp32
+ * accumulate and output.  desc: a TP_W_VOCAB buffer; x: [M, d] bf16; logits: [M, vocab] fp32
+ * (padding ids are not written).  ws optional as for tp_colpar_forward.  M == 0 is a no-op. */
+tp_status tp_lm_head_forward(const tp_packed_desc* desc /* host */, const void* w, const void* x, int32_t M,
+                             float* logits, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
+
+/* Vocabulary-parallel embedding lookup (the table split by vocabulary rows; each shard contributes
+ * its row if the id is in its range, else zeros, and the contributions are summed, which leaves
+ * exactly one row): x[m] = E[ids[m]], a zero row for an id outside [0, vocab).  desc: a
+ * TP_W_EMBED buffer; ids: [M] int32 (device); x: [M, d] bf16.  M == 0 is a no-op. */
+tp_status tp_embed_lookup(const tp_packed_desc* desc /* host */, const void* w, const int32_t* ids, int32_t M,
+                          void* x, void* stream);
 
 /* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g). */
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,

@@ -32,12 +32,18 @@ inline int k_chunk(int wtype) { return wtype == TP_FP8_E4M3 ? 64 : 32; }
 
 tp_status check_shape(const tp_shape* sh, int kind) {
   if (!sh) return TP_ERR_INVALID_ARG;
-  if (kind < TP_W_GATE_UP || kind > TP_W_O) return TP_ERR_INVALID_ARG;
+  if (kind < TP_W_GATE_UP || kind > TP_W_EMBED) return TP_ERR_INVALID_ARG;
   if (sh->wtype != TP_BF16 && sh->wtype != TP_FP8_E4M3) return TP_ERR_INVALID_ARG;
   const int t = sh->t;
   if (t != 1 && t != 2 && t != 4 && t != 8) return TP_ERR_SHAPE;
   if (sh->d <= 0) return TP_ERR_SHAPE;
   if (sh->d % 32) return TP_ERR_ALIGN;
+  if (kind == TP_W_VOCAB || kind == TP_W_EMBED) {
+    if (sh->vocab <= 0) return TP_ERR_SHAPE;
+    if (sh->wtype != TP_BF16) return TP_ERR_UNSUPPORTED;  // the vocabulary edges are bf16 only
+    if (sh->d % 64) return TP_ERR_ALIGN;                   // 64-wide k-blocks of the lm_head GEMM
+    return TP_OK;
+  }
   const int kc = k_chunk(sh->wtype);
   if (kind == TP_W_GATE_UP || kind == TP_W_DOWN) {
     if (sh->ffn <= 0 || sh->ffn % t) return TP_ERR_SHAPE;
@@ -67,6 +73,14 @@ void geometry(const tp_shape* sh, int kind, int64_t* rows, int64_t* K, int64_t* 
       *K = sh->d;
       *out_cols = (int64_t)(sh->n_q_heads + 2 * sh->n_kv_heads) * sh->head_dim;
       break;
+    case TP_W_VOCAB:
+    case TP_W_EMBED: {
+      const int64_t q = 128LL * t, vp = ((int64_t)sh->vocab + q - 1) / q * q;  // padded vocabulary
+      *rows = vp / t;
+      *K = sh->d;
+      *out_cols = kind == TP_W_VOCAB ? sh->vocab : sh->d;
+      break;
+    }
     default:
       *rows = sh->d; *K = (int64_t)sh->n_q_heads / t * sh->head_dim; *out_cols = sh->d; break;
   }
@@ -191,7 +205,8 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
   if (packed_bytes < d.total_bytes) return TP_ERR_INVALID_ARG;
   PackGeom g{};
   g.kind = kind;
-  g.colpar = kind == TP_W_GATE_UP || kind == TP_W_QKV;
+  g.colpar = kind == TP_W_GATE_UP || kind == TP_W_QKV || kind == TP_W_VOCAB;
+  g.vocab = shape->vocab;
   g.fp8 = shape->wtype == TP_FP8_E4M3;
   g.t = shape->t;
   int64_t rows, K, oc;
@@ -701,6 +716,45 @@ tp_status tp_layer_forward(const tp_packed_desc* qkv, const void* qkv_w, const t
   st = tp_rmsnorm(h1, nullptr, eps, M, (int32_t)d, b, stream);
   if (st != TP_OK) return st;
   return tp_mlp_forward(gu, gu_w, dn, dn_w, b, h1, M, y, h, ws, ws_bytes, flags, stream);
+}
+
+tp_status tp_lm_head_forward(const tp_packed_desc* desc, const void* w, const void* x, int32_t M, float* logits,
+                             void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  tp_status st = check_desc(desc, TP_W_VOCAB, w);
+  if (st != TP_OK) return st;
+  if ((flags & ~(TP_F_SERIAL | TP_F_KERNEL_TC)) != 0) return TP_ERR_INVALID_ARG;
+  if (M < 0 || (M > 0 && (!x || !logits))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x) || !aligned16(logits)) return TP_ERR_ALIGN;
+  const int rows = (int)desc->rows_per_shard, K = (int)desc->k_per_shard;
+  if (!tc_supported(rows, K, false)) return TP_ERR_UNSUPPORTED;
+  TcArgs a{};
+  a.mode = TC_COLPAR_F32;
+  a.w = static_cast<const uint8_t*>(w);
+  a.shard_stride = desc->shard_stride_bytes;
+  a.t = desc->shape.t;
+  a.rows = rows;
+  a.K = K;
+  a.x = static_cast<const bf16*>(x);
+  a.ldx = K;
+  a.M = M;
+  a.out = logits;
+  a.ldo = desc->shape.vocab;  // the shards' slices, concatenated, cut to the real ids
+  a.ncols = desc->shape.vocab;
+  if (ws && aligned16(ws) && ws_bytes >= sk_bytes()) set_streamk(a, ws);
+  return launch_tc(a, S(stream), (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+}
+
+tp_status tp_embed_lookup(const tp_packed_desc* desc, const void* w, const int32_t* ids, int32_t M, void* x,
+                          void* stream) {
+  tp_status st = check_desc(desc, TP_W_EMBED, w);
+  if (st != TP_OK) return st;
+  if (M < 0 || (M > 0 && (!ids || !x))) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!aligned16(x)) return TP_ERR_ALIGN;
+  return cuda_status(launch_embed(static_cast<const uint8_t*>(w), desc->shard_stride_bytes,
+                                  (int)desc->rows_per_shard, desc->shape.t, desc->shape.vocab, desc->shape.d, ids,
+                                  M, static_cast<bf16*>(x), S(stream)));
 }
 
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,

@@ -14,6 +14,10 @@ namespace tpx {
 
 // Unsharded source column (and which matrix) of packed row r of shard s.
 __device__ __forceinline__ int colpar_src(const PackGeom& g, int s, int r, int* which) {
+  if (g.kind == TP_W_VOCAB) {  // vocabulary id s*V_s + r (>= vocab: a padding row)
+    *which = 0;
+    return s * g.rows + r;
+  }
   if (g.kind == TP_W_GATE_UP) {
     const int fs = g.ffn / g.t;
     const int blk = r >> 4, j = r & 15;
@@ -30,8 +34,15 @@ __device__ __forceinline__ int colpar_src(const PackGeom& g, int s, int r, int* 
   return (g.n_q + g.n_kv) * hd + s * nkvs * hd + r;
 }
 
+// Whether packed row r of shard s has a source (padding rows of the vocabulary do not).
+__device__ __forceinline__ bool src_valid(const PackGeom& g, int s, int r) {
+  return (g.kind != TP_W_VOCAB && g.kind != TP_W_EMBED) || s * g.rows + r < g.vocab;
+}
+
 // Map (shard s, packed row r, k) -> element of the [in, out] source.
 __device__ __forceinline__ const uint16_t* src_elem(const PackGeom& g, int s, int r, int k) {
+  if (g.kind == TP_W_EMBED)  // rows of the [vocab, d] table as they are
+    return g.W0 + (size_t)(s * g.rows + r) * g.K + k;
   if (g.colpar) {
     int which;
     const int col = colpar_src(g, s, r, &which);
@@ -90,7 +101,7 @@ __global__ void pack_kernel(PackGeom g, uint8_t* packed) {
   for (int kk = threadIdx.y; kk < 32; kk += 8) {
     const int r = r0 + threadIdx.x, k = k0 + kk;
     uint16_t v = 0;
-    if (r < g.rows && k < g.K) v = *src_elem(g, s, r, k);
+    if (r < g.rows && k < g.K && src_valid(g, s, r)) v = *src_elem(g, s, r, k);
     tile[kk][threadIdx.x] = v;
   }
   __syncthreads();

@@ -132,6 +132,28 @@ cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows,
   return cudaGetLastError();
 }
 
+// Vocabulary-parallel embedding: each shard owns the ids of its range; for a token only the
+// owning shard contributes a row and the others contribute zeros, so the sum over shards is
+// that row, copied here directly.  One CTA per token, 16 bytes per thread per step.
+__global__ void embed_kernel(const uint8_t* __restrict__ table, uint64_t stride, int vs, int t, int vocab, int d,
+                             const int32_t* __restrict__ ids, __nv_bfloat16* __restrict__ x) {
+  const int m = blockIdx.x;
+  const int id = ids[m];
+  const bool ok = id >= 0 && id < vocab && id / vs < t;
+  const uint4* src = ok ? reinterpret_cast<const uint4*>(table + (size_t)(id / vs) * stride +
+                                                         (size_t)(id % vs) * d * 2)
+                        : nullptr;
+  uint4* dst = reinterpret_cast<uint4*>(x + (size_t)m * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = ok ? src[i] : make_uint4(0, 0, 0, 0);
+}
+
+cudaError_t launch_embed(const uint8_t* table, uint64_t stride, int vs, int t, int vocab, int d, const int32_t* ids,
+                         int M, __nv_bfloat16* x, cudaStream_t st) {
+  embed_kernel<<<M, 128, 0, st>>>(table, stride, vs, t, vocab, d, ids, x);
+  note_launch();
+  return cudaGetLastError();
+}
+
 __global__ void attn1_kernel(const __nv_bfloat16* __restrict__ qkv, int M, int n_q, int n_kv, int hd,
                              int t, __nv_bfloat16* o_in) {
   const int nqs = n_q / t, nkvs = n_kv / t, group = n_q / n_kv;

@@ -14,6 +14,10 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, fl
 // in the same per-shard layout, shards packed densely (shard s at s * rows * K elements).
 cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows, int K, int t, __nv_bfloat16* dst,
                               cudaStream_t st);
+// x[m] = row ids[m] of the vocabulary-split table (shard ids[m] / vs, row ids[m] % vs; shard s at
+// s * stride bytes, rows of d bf16), or zeros for an id outside [0, vocab).
+cudaError_t launch_embed(const uint8_t* table, uint64_t stride, int vs, int t, int vocab, int d, const int32_t* ids,
+                         int M, __nv_bfloat16* x, cudaStream_t st);
 cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
                          __nv_bfloat16* o_in, cudaStream_t st);
 

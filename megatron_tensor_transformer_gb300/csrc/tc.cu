@@ -163,6 +163,7 @@ __device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, in
     }
   } else if (a.mode == TC_COLPAR_BF16 || a.mode == TC_COLPAR_F32) {
     const size_t col = (size_t)s * a.rows + p;
+    if (a.ncols && col >= (size_t)a.ncols) return;
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       if (mf + j >= a.M) break;
@@ -229,6 +230,7 @@ __device__ __forceinline__ void emit(const TcArgs& a, int s, int rt, int row, in
     const int f = s * (a.rows / 2) + (p >> 4) * 8 + (p & 7);
     reinterpret_cast<uint16_t*>(a.out)[(size_t)m * a.ldo + f] = f2bf(silu_f(v) * u);
   } else if (a.mode == TC_COLPAR_BF16 || a.mode == TC_COLPAR_F32) {
+    if (a.ncols && (size_t)s * a.rows + p >= (size_t)a.ncols) return;
     const size_t o = (size_t)m * a.ldo + (size_t)s * a.rows + p;
     if (a.mode == TC_COLPAR_F32)
       reinterpret_cast<float*>(a.out)[o] = v;

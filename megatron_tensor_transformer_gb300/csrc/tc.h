@@ -28,6 +28,7 @@ struct TcArgs {
   int ldx, M;
   void* out;                 // colpar output
   int ldo;
+  int ncols;                 // colpar: columns to write (0 = all); padded vocabulary ids are not
   // row-parallel
   const __nv_bfloat16* residual;  // nullable, [M, ldy]
   __nv_bfloat16* y;               // [M, ldy]

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(_PKG, "libtpx.so")
 TP_OK, TP_ERR_INVALID_ARG, TP_ERR_SHAPE, TP_ERR_ALIGN, TP_ERR_LAYOUT_MISMATCH = 0, 1, 2, 3, 4
 TP_ERR_WORKSPACE, TP_ERR_CUDA, TP_ERR_TIMEOUT, TP_ERR_DEVICE_TIMEOUT, TP_ERR_UNSUPPORTED = 5, 6, 7, 8, 9
 TP_BF16, TP_FP8_E4M3 = 0, 1
-TP_W_GATE_UP, TP_W_DOWN, TP_W_QKV, TP_W_O = 0, 1, 2, 3
+TP_W_GATE_UP, TP_W_DOWN, TP_W_QKV, TP_W_O, TP_W_VOCAB, TP_W_EMBED = 0, 1, 2, 3, 4, 5
 TP_F_UNFUSED_REDUCE, TP_F_FP32_COLPAR_OUT = 0x1, 0x2
 TP_F_KERNEL_SKINNY, TP_F_KERNEL_TC, TP_F_SERIAL, TP_F_SPLIT_BLOCK = 0x10, 0x20, 0x40, 0x80
 
@@ -23,7 +23,8 @@ EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspa
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
            "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
-           "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count"]
+           "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count",
+           "tp_lm_head_forward", "tp_embed_lookup"]
 
 
 class TpxError(RuntimeError):
@@ -35,7 +36,7 @@ class TpxError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("d", ctypes.c_int32), ("ffn", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("t", ctypes.c_int32),
-                ("wtype", ctypes.c_int32)]
+                ("wtype", ctypes.c_int32), ("vocab", ctypes.c_int32)]
 
 
 class PackedDesc(ctypes.Structure):
@@ -78,6 +79,8 @@ def lib():
             "tp_layer_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V, P(PackedDesc), V,
                                        V, I32, V, ctypes.c_float, V, SZ, V, SZ, U32, V]),
             "tp_status_str": (ctypes.c_char_p, [I32]),
+            "tp_lm_head_forward": (I32, [P(PackedDesc), V, V, I32, V, V, SZ, U32, V]),
+            "tp_embed_lookup": (I32, [P(PackedDesc), V, V, I32, V, V]),
             "tp_launch_count": (ctypes.c_uint64, []),
         }
         for name, (res, args) in sig.items():
@@ -108,8 +111,8 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def make_shape(d, ffn=0, n_q=0, n_kv=0, hd=0, t=1, wtype=TP_BF16):
-    return Shape(d, ffn, n_q, n_kv, hd, t, wtype)
+def make_shape(d, ffn=0, n_q=0, n_kv=0, hd=0, t=1, wtype=TP_BF16, vocab=0):
+    return Shape(d, ffn, n_q, n_kv, hd, t, wtype, vocab)
 
 
 def tp_packed_bytes(shape, kind):
@@ -234,3 +237,16 @@ def tp_selftest_e4m3_decode(codes, out, stream=None):
 
 def tp_launch_count():
     return lib().tp_launch_count()
+
+
+def tp_lm_head_forward(desc, w, x, logits, ws=None, flags=0, stream=None):
+    _check(lib().tp_lm_head_forward(ctypes.byref(desc), _ptr(w), _ptr(x), x.shape[0], _ptr(logits), _ptr(ws),
+                                    0 if ws is None else ws.numel(), flags, _stream(stream)), "tp_lm_head_forward")
+    return logits
+
+
+def tp_embed_lookup(desc, w, ids, x, stream=None):
+    _check(lib().tp_embed_lookup(ctypes.byref(desc), _ptr(w), _ptr(ids), ids.shape[0], _ptr(x), _stream(stream)),
+           "tp_embed_lookup")
+    return x
+
