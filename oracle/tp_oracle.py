@@ -181,6 +181,50 @@ def attention_one_token(qkv, n_q, n_kv, hd):
     return out
 
 
+def attention_decode(qkv, k_cache, v_cache, lens, n_q, n_kv, hd):
+    """Decode attention over a KV cache, one new token per sequence m (grouped-query: q head h
+    reads kv head floor(h / (n_q / n_kv))).  The token's own k and v are the cache's entry at
+    position lens[m]; it attends over positions 0..lens[m]:
+        o[m, h] = sum_j softmax_j(q[m, h] . k[m, g, j] / sqrt(hd)) v[m, g, j].
+    qkv: [M, (n_q + 2 n_kv) hd] in the unsharded column order [q | k | v]; k_cache, v_cache:
+    [M, n_kv, L, hd] with the new token's k and v already at position lens[m].  Returns o_in
+    [M, n_q hd].  A sequence with lens[m] outside [0, L) gets a zero row."""
+    qkv = as_f64(qkv)
+    k_cache, v_cache = as_f64(k_cache), as_f64(v_cache)
+    M = qkv.shape[0]
+    group = n_q // n_kv
+    L = k_cache.shape[2]
+    out = np.zeros((M, n_q * hd))
+    for m in range(M):
+        n = int(lens[m])
+        if n < 0 or n >= L:
+            continue
+        for h in range(n_q):
+            g = h // group
+            q = qkv[m, h * hd:(h + 1) * hd]
+            sc = k_cache[m, g, :n + 1] @ q / np.sqrt(hd)
+            p = np.exp(sc - sc.max())
+            p /= p.sum()
+            out[m, h * hd:(h + 1) * hd] = p @ v_cache[m, g, :n + 1]
+    return out
+
+
+def append_kv(qkv, k_cache, v_cache, lens, n_q, n_kv, hd):
+    """Copies of the caches with the new token's k and v (from qkv) written at position
+    lens[m] of every kv head; sequences with lens[m] outside [0, L) are left as they are."""
+    qkv = np.asarray(qkv)
+    k2, v2 = np.array(k_cache, copy=True), np.array(v_cache, copy=True)
+    L = k2.shape[2]
+    for m in range(qkv.shape[0]):
+        n = int(lens[m])
+        if n < 0 or n >= L:
+            continue
+        for g in range(n_kv):
+            k2[m, g, n] = qkv[m, (n_q + g) * hd:(n_q + g + 1) * hd]
+            v2[m, g, n] = qkv[m, (n_q + n_kv + g) * hd:(n_q + n_kv + g + 1) * hd]
+    return k2, v2
+
+
 def proj(x, w_qkv, w_o, n_q, n_kv, hd, residual=None):
     """Attention sub-block with the one-token attention stand-in:
     qkv = x Wqkv;  o_in = attention(qkv);  y = residual + o_in Wo.  Returns (y, qkv)."""

@@ -365,3 +365,77 @@ def test_embedding_lookup_by_hand_and_vocab_parallel_sum():
     shards = O.pack_embed(e, 2)
     np.testing.assert_array_equal(shards[0][:V], e)
     assert not shards[0][V:].any() and not shards[1].any()
+
+
+# ---------------------------------------------------------------- decode attention over a KV cache
+
+def _attn_case(M=3, n_q=4, n_kv=2, hd=8, L=6, seed=0):
+    rng = np.random.default_rng(seed)
+    qkv = rng.normal(size=(M, (n_q + 2 * n_kv) * hd))
+    kc = rng.normal(size=(M, n_kv, L, hd))
+    vc = rng.normal(size=(M, n_kv, L, hd))
+    return qkv, kc, vc
+
+
+def test_attention_with_empty_history_is_the_one_token_stand_in():
+    """lens = 0: the only position is the token itself, softmax over one score is 1, so every
+    q head returns its group's v: the one-token attention stand-in."""
+    n_q, n_kv, hd = 4, 2, 8
+    qkv, kc, vc = _attn_case(n_q=n_q, n_kv=n_kv, hd=hd)
+    lens = [0, 0, 0]
+    k2, v2 = O.append_kv(qkv, kc, vc, lens, n_q, n_kv, hd)
+    np.testing.assert_allclose(O.attention_decode(qkv, k2, v2, lens, n_q, n_kv, hd),
+                               O.attention_one_token(qkv, n_q, n_kv, hd), rtol=0, atol=1e-15)
+
+
+def test_attention_equal_keys_average_the_values():
+    """All keys equal: every score is the same, softmax is uniform, o is the mean of v."""
+    n_q, n_kv, hd = 2, 1, 4
+    qkv, kc, vc = _attn_case(M=1, n_q=n_q, n_kv=n_kv, hd=hd, L=5)
+    kc[:] = 0.5
+    qkv[0, n_q * hd:(n_q + 1) * hd] = 0.5          # the new token's k, equal too
+    lens = [3]
+    k2, v2 = O.append_kv(qkv, kc, vc, lens, n_q, n_kv, hd)
+    o = O.attention_decode(qkv, k2, v2, lens, n_q, n_kv, hd)
+    mean_v = v2[0, 0, :4].mean(axis=0)
+    np.testing.assert_allclose(o[0, :hd], mean_v, rtol=1e-13)
+    np.testing.assert_allclose(o[0, hd:], mean_v, rtol=1e-13)
+
+
+def test_attention_brute_force_and_out_of_range_lengths():
+    n_q, n_kv, hd, L = 4, 2, 3, 5
+    qkv, kc, vc = _attn_case(M=3, n_q=n_q, n_kv=n_kv, hd=hd, L=L, seed=3)
+    lens = [2, 4, 5]                                # the last is out of range: a zero row
+    k2, v2 = O.append_kv(qkv, kc, vc, lens, n_q, n_kv, hd)
+    o = O.attention_decode(qkv, k2, v2, lens, n_q, n_kv, hd)
+    assert not o[2].any()
+    np.testing.assert_array_equal(k2[2], kc[2])     # nothing appended out of range
+    for m in range(2):
+        for h in range(n_q):
+            g = h // (n_q // n_kv)
+            q = [qkv[m, h * hd + i] for i in range(hd)]
+            sc = [sum(q[i] * k2[m, g, j, i] for i in range(hd)) / hd ** 0.5 for j in range(lens[m] + 1)]
+            e = [np.exp(v - max(sc)) for v in sc]
+            ref = [sum(e[j] * v2[m, g, j, i] for j in range(lens[m] + 1)) / sum(e) for i in range(hd)]
+            np.testing.assert_allclose(o[m, h * hd:(h + 1) * hd], ref, rtol=1e-12)
+    # the appended entries are the token's k and v
+    np.testing.assert_array_equal(k2[1, 1, 4], qkv[1, (n_q + 1) * hd:(n_q + 2) * hd])
+    np.testing.assert_array_equal(v2[0, 0, 2], qkv[0, (n_q + n_kv) * hd:(n_q + n_kv + 1) * hd])
+
+
+@pytest.mark.parametrize("t", [1, 2])
+def test_attention_head_sharded_equals_unsharded(t):
+    """Each shard attends with its own q heads over its own kv heads (whole GQA groups): the
+    per-shard outputs, placed at their heads, are the unsharded output."""
+    n_q, n_kv, hd = 4, 2, 8
+    qkv, kc, vc = _attn_case(n_q=n_q, n_kv=n_kv, hd=hd, seed=5)
+    lens = [1, 3, 5]
+    k2, v2 = O.append_kv(qkv, kc, vc, lens, n_q, n_kv, hd)
+    full = O.attention_decode(qkv, k2, v2, lens, n_q, n_kv, hd)
+    nqs, nkvs = n_q // t, n_kv // t
+    for s in range(t):
+        cols = O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0]
+        qkv_s = qkv[:, cols]
+        o_s = O.attention_decode(qkv_s, k2[:, s * nkvs:(s + 1) * nkvs], v2[:, s * nkvs:(s + 1) * nkvs], lens,
+                                 nqs, nkvs, hd)
+        np.testing.assert_allclose(o_s, full[:, s * nqs * hd:(s + 1) * nqs * hd], rtol=0, atol=0)
