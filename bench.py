@@ -539,6 +539,75 @@ def run_lm_head(args, rank, world, local):
         "gpu_launches": launches, "clocks": clk.summary()}), flush=True)
 
 
+def run_attn(args, rank, world, local):
+    """Llama-3.1 70B attention block with a real KV cache: 32 sequences, each with 4095 cached
+    positions (4096 with the new token), t=8.  One step = QKV (column-parallel) + the
+    head-sharded decode attention over the cache + o_proj (row-parallel, shard fold, residual).
+    The roofline kernel is the attention (cache reads: M x n_kv x 4096 x hd x 2 x 2 bytes)."""
+    import torch
+    from megatron_tensor_transformer_gb300 import inputs, tpx
+
+    d, n_q, n_kv, hd, t, M, L = 8192, 64, 8, 128, args.t or 8, 32, 4096
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
+    x, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, M, seed=0, device=dev)
+    q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv, stream=stream)
+    o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo, stream=stream)
+    del wqkv, wo
+    kc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, 0, 90, dev)
+    vc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, 0, 91, dev)
+    lens = torch.full((M,), L - 1, dtype=torch.int32, device=dev)
+    qkv = torch.empty((M, (n_q + 2 * n_kv) * hd), dtype=torch.bfloat16, device=dev)
+    o_in = torch.empty((M, n_q * hd), dtype=torch.bfloat16, device=dev)
+    y = torch.empty_like(x)
+    ws = tpx.new_workspace(sh, M, dev)
+    aws = torch.empty(tpx.tp_attn_workspace_bytes(sh, M, L), dtype=torch.uint8, device=dev)
+    K = args.steps
+
+    def step():
+        tpx.tp_colpar_forward(q, q_w, x, qkv, ws=ws, stream=stream)
+        tpx.tp_attn_decode(sh, qkv, kc, vc, lens, o_in, aws, stream=stream)
+        tpx.tp_rowpar_forward(o, o_w, o_in, x, y, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        stream.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n0 = tpx.tp_launch_count()
+        with Clocks(f"/tmp/tpx_clocks_{os.getpid()}.csv") as clk:
+            a.record(stream)
+            for _ in range(K):
+                step()
+            b.record(stream)
+            b.synchronize()
+        launches = tpx.tp_launch_count() - n0
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(K):
+            tpx.tp_attn_decode(sh, qkv, kc, vc, lens, o_in, aws, stream=stream)
+        c1.record(stream)
+        c1.synchronize()
+    ms, attn_ms = a.elapsed_time(b) / K, c0.elapsed_time(c1) / K
+    cache_bytes = 2.0 * M * n_kv * L * hd * 2
+    w_bytes = 2.0 * ((n_q + 2 * n_kv) * hd * d + n_q * hd * d)
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+        pk = json.load(f)
+    print(json.dumps({
+        "metric": METRIC, "workload": "70b-attn-decode", "value": M / (ms * 1e-3), "unit": "tokens/s",
+        "higher_is_better": True, "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": ms,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "70b-attn-decode", "d": d, "n_q": n_q, "n_kv": n_kv, "head_dim": hd, "t": t,
+                   "M": M, "context": L},
+        "hbm_gbs_step": (cache_bytes + w_bytes) / (ms * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "decode attention (append + chunks + combine)",
+                     "achieved": cache_bytes / (attn_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": cache_bytes / (attn_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "attn_us": 1e3 * attn_ms},
+        "gpu_launches": launches, "clocks": clk.summary()}), flush=True)
+
+
 def run_e2e(args, gu, gu_w, dn, dn_w, sh, dev):
     """Through the public C-ABI call tp_mlp_forward with HOST buffers: every step copies each
     batch's x from pinned host memory, runs the block, and copies y back."""
@@ -583,7 +652,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", default="8b-mlp-decode",
-                    choices=["8b-mlp-decode", "405b-stack-decode", "70b-lm-head-decode"] + sorted(LAYERS),
+                    choices=["8b-mlp-decode", "405b-stack-decode", "70b-lm-head-decode", "70b-attn-decode"] +
+                    sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny", "split"],
@@ -597,6 +667,8 @@ def main():
         run_stack(args, rank, world, local)
     elif args.workload == "70b-lm-head-decode":
         run_lm_head(args, rank, world, local)
+    elif args.workload == "70b-attn-decode":
+        run_attn(args, rank, world, local)
     elif args.workload != "8b-mlp-decode":
         run_layer(args, rank, world, local)
     elif args.impl == "reference":

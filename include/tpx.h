@@ -227,6 +227,23 @@ tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc /* host */, const
 /* Bytes of the static scratch array tp_rowpar_forward_noalloc uses. */
 size_t tp_noalloc_scratch_capacity(void);
 
+/* Decode attention over a KV cache, head-sharded (each shard attends with its own q heads over
+ * the cache of its own kv heads, whole GQA groups, "local attention over this GPU's heads",
+ * scalablesystem.dev "The Tensor-Parallel Shard Group"; "the KV cache splits too", vidyal.ai).
+ * One new token per sequence m: its k and v (from qkv) are first written into the cache at
+ * position lens[m]; then, for q head h and its kv head g = h / (n_q / n_kv),
+ *   o_in[m][h*hd + i] = bf16( sum_j softmax_j(q . k_j / sqrt(hd)) v_j[i] ),  j = 0 .. lens[m],
+ * with fp32 scores, softmax and accumulation (no positional rotation: the pages give none).
+ * qkv: [M, (n_q + 2 n_kv) hd] bf16 in the column-parallel shard-major order (tp_colpar_forward's
+ * QKV output); k_cache, v_cache: [t][M][n_kv/t][L][hd] bf16 (device, caller-owned; shard s holds
+ * its kv heads' cache); lens: [M] int32 (device, not modified); o_in: [M, n_q hd] bf16 (the
+ * row-parallel o_proj input).  A sequence with lens[m] outside [0, L) is left out: nothing is
+ * written to its cache and its o_in row is zero.  head_dim must be 64, 128 or 256.
+ * ws: tp_attn_workspace_bytes(shape, M, L) bytes (no zero-fill needed). */
+size_t tp_attn_workspace_bytes(const tp_shape* shape /* host */, int32_t M, int32_t L);
+tp_status tp_attn_decode(const tp_shape* shape /* host */, const void* qkv, void* k_cache, void* v_cache, int32_t L,
+                         const int32_t* lens, int32_t M, void* o_in, void* ws, size_t ws_bytes, void* stream);
+
 /* Vocabulary-parallel lm_head (the column-parallel GEMM at the model's output edge; each shard's
  * logits are a slice of the output, so the pages' all-gather is a concatenation, scalablesystem.dev
  * "The Tensor-Parallel Shard Group"): logits[m][v] = sum_k x[m][k] W[k][v] for v < vocab, fp32

@@ -6,6 +6,7 @@
 #include <cstring>
 #include <thread>
 
+#include "attn.h"
 #include "common.cuh"
 #include "fused.h"
 #include "pack.h"
@@ -716,6 +717,30 @@ tp_status tp_layer_forward(const tp_packed_desc* qkv, const void* qkv_w, const t
   st = tp_rmsnorm(h1, nullptr, eps, M, (int32_t)d, b, stream);
   if (st != TP_OK) return st;
   return tp_mlp_forward(gu, gu_w, dn, dn_w, b, h1, M, y, h, ws, ws_bytes, flags, stream);
+}
+
+size_t tp_attn_workspace_bytes(const tp_shape* sh, int32_t M, int32_t L) {
+  if (!sh || M < 0 || L <= 0 || check_shape(sh, TP_W_QKV) != TP_OK) return 0;
+  return attn_workspace_bytes(sh->t, M, L, sh->n_q_heads, sh->n_kv_heads, sh->head_dim);
+}
+
+tp_status tp_attn_decode(const tp_shape* sh, const void* qkv, void* k_cache, void* v_cache, int32_t L,
+                         const int32_t* lens, int32_t M, void* o_in, void* ws, size_t ws_bytes, void* stream) {
+  tp_status st = check_shape(sh, TP_W_QKV);
+  if (st != TP_OK) return st;
+  if (M < 0 || L <= 0) return TP_ERR_INVALID_ARG;
+  if (!attn_supported(sh->head_dim, sh->n_q_heads / sh->n_kv_heads)) return TP_ERR_UNSUPPORTED;
+  if (M == 0) return TP_OK;
+  if (!qkv || !k_cache || !v_cache || !lens || !o_in || !ws) return TP_ERR_INVALID_ARG;
+  if (!aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_in) || !aligned16(ws))
+    return TP_ERR_ALIGN;
+  if (ws_bytes < tp_attn_workspace_bytes(sh, M, L)) return TP_ERR_WORKSPACE;
+  unsigned* err = tc_error_word();
+  if (!err) return TP_ERR_CUDA;
+  return cuda_status(launch_attn_decode(sh->t, M, L, sh->n_q_heads, sh->n_kv_heads, sh->head_dim,
+                                        static_cast<const bf16*>(qkv), static_cast<bf16*>(k_cache),
+                                        static_cast<bf16*>(v_cache), lens, static_cast<bf16*>(o_in),
+                                        static_cast<float*>(ws), err, S(stream)));
 }
 
 tp_status tp_lm_head_forward(const tp_packed_desc* desc, const void* w, const void* x, int32_t M, float* logits,

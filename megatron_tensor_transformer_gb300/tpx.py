@@ -24,7 +24,7 @@ EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspa
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
            "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
            "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count",
-           "tp_lm_head_forward", "tp_embed_lookup"]
+           "tp_lm_head_forward", "tp_embed_lookup", "tp_attn_workspace_bytes", "tp_attn_decode"]
 
 
 class TpxError(RuntimeError):
@@ -81,6 +81,8 @@ def lib():
             "tp_status_str": (ctypes.c_char_p, [I32]),
             "tp_lm_head_forward": (I32, [P(PackedDesc), V, V, I32, V, V, SZ, U32, V]),
             "tp_embed_lookup": (I32, [P(PackedDesc), V, V, I32, V, V]),
+            "tp_attn_workspace_bytes": (SZ, [P(Shape), I32, I32]),
+            "tp_attn_decode": (I32, [P(Shape), V, V, V, I32, V, I32, V, V, SZ, V]),
             "tp_launch_count": (ctypes.c_uint64, []),
         }
         for name, (res, args) in sig.items():
@@ -249,4 +251,16 @@ def tp_embed_lookup(desc, w, ids, x, stream=None):
     _check(lib().tp_embed_lookup(ctypes.byref(desc), _ptr(w), _ptr(ids), ids.shape[0], _ptr(x), _stream(stream)),
            "tp_embed_lookup")
     return x
+
+
+def tp_attn_workspace_bytes(shape, M, L):
+    return lib().tp_attn_workspace_bytes(ctypes.byref(shape), M, L)
+
+
+def tp_attn_decode(shape, qkv, k_cache, v_cache, lens, o_in, ws, stream=None):
+    """k_cache, v_cache: [t, M, n_kv/t, L, hd] bf16; lens: [M] int32 on the device."""
+    L = k_cache.shape[3]
+    _check(lib().tp_attn_decode(ctypes.byref(shape), _ptr(qkv), _ptr(k_cache), _ptr(v_cache), L, _ptr(lens),
+                                qkv.shape[0], _ptr(o_in), _ptr(ws), ws.numel(), _stream(stream)), "tp_attn_decode")
+    return o_in
 
