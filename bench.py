@@ -602,7 +602,7 @@ def run_attn(args, rank, world, local):
         "config": {"workload": "70b-attn-decode", "d": d, "n_q": n_q, "n_kv": n_kv, "head_dim": hd, "t": t,
                    "M": M, "context": L},
         "hbm_gbs_step": (cache_bytes + w_bytes) / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "decode attention (append + chunks + combine)",
+        "roofline": {"bound": "hbm", "kernel": "decode attention (append + attention pass)",
                      "achieved": cache_bytes / (attn_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                      "frac": cache_bytes / (attn_ms * 1e-3) / 1e9 / pk["hbm_gbs"], "attn_us": 1e3 * attn_ms},
         "gpu_launches": launches, "clocks": clk.summary()}), flush=True)

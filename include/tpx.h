@@ -233,13 +233,20 @@ size_t tp_noalloc_scratch_capacity(void);
  * One new token per sequence m: its k and v (from qkv) are first written into the cache at
  * position lens[m]; then, for q head h and its kv head g = h / (n_q / n_kv),
  *   o_in[m][h*hd + i] = bf16( sum_j softmax_j(q . k_j / sqrt(hd)) v_j[i] ),  j = 0 .. lens[m],
- * with fp32 scores, softmax and accumulation (no positional rotation: the pages give none).
+ * with fp32 scores, softmax and accumulation; the probabilities enter the p.v product rounded
+ * to bf16, the tensor cores' operand type (no positional rotation: the pages give none).
  * qkv: [M, (n_q + 2 n_kv) hd] bf16 in the column-parallel shard-major order (tp_colpar_forward's
  * QKV output); k_cache, v_cache: [t][M][n_kv/t][L][hd] bf16 (device, caller-owned; shard s holds
  * its kv heads' cache); lens: [M] int32 (device, not modified); o_in: [M, n_q hd] bf16 (the
  * row-parallel o_proj input).  A sequence with lens[m] outside [0, L) is left out: nothing is
- * written to its cache and its o_in row is zero.  head_dim must be 64, 128 or 256.
- * ws: tp_attn_workspace_bytes(shape, M, L) bytes (no zero-fill needed). */
+ * written to its cache and its o_in row is zero.  head_dim must be 64, 128 or 256, n_q / n_kv at
+ * most 16 and M * n_kv * L below 2^31 (else TP_ERR_UNSUPPORTED); qkv, the caches, o_in and ws
+ * 16-byte aligned (else TP_ERR_ALIGN).  Cache slots after lens[m] are never read into the result.
+ * ws: tp_attn_workspace_bytes(shape, M, L) bytes, partial results per 128-position chunk and a
+ * merge counter per (sequence, kv head), which the call resets itself (no zero-fill needed);
+ * calls that share a ws must not overlap on the GPU.  Two kernel launches; the result is
+ * bitwise the same run to run.  A staged copy that never lands sets the device error word
+ * (TP_ERR_DEVICE_TIMEOUT from tp_sync). */
 size_t tp_attn_workspace_bytes(const tp_shape* shape /* host */, int32_t M, int32_t L);
 tp_status tp_attn_decode(const tp_shape* shape /* host */, const void* qkv, void* k_cache, void* v_cache, int32_t L,
                          const int32_t* lens, int32_t M, void* o_in, void* ws, size_t ws_bytes, void* stream);

@@ -730,6 +730,7 @@ tp_status tp_attn_decode(const tp_shape* sh, const void* qkv, void* k_cache, voi
   if (st != TP_OK) return st;
   if (M < 0 || L <= 0) return TP_ERR_INVALID_ARG;
   if (!attn_supported(sh->head_dim, sh->n_q_heads / sh->n_kv_heads)) return TP_ERR_UNSUPPORTED;
+  if ((int64_t)M * sh->n_kv_heads * L >= (int64_t(1) << 31)) return TP_ERR_UNSUPPORTED;  // cache rows: int32
   if (M == 0) return TP_OK;
   if (!qkv || !k_cache || !v_cache || !lens || !o_in || !ws) return TP_ERR_INVALID_ARG;
   if (!aligned16(qkv) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o_in) || !aligned16(ws))

@@ -7,9 +7,9 @@
 
 namespace tpx {
 
-// fp32 workspace bytes of the per-chunk partial results
+// workspace bytes: fp32 per-chunk partial results, then a merge counter per (sequence, kv head)
 size_t attn_workspace_bytes(int t, int M, int L, int n_q, int n_kv, int hd);
-// head dim 64, 128 or 256; q heads per kv head 1..64
+// head dim 64, 128 or 256; q heads per kv head 1..16 (the rows of one MMA tile)
 bool attn_supported(int hd, int G);
 // append the new k, v of qkv [M, Q] (shard-major) at position lens[m], then o_in [M, n_q hd] =
 // attention over positions 0..lens[m]; caches [t][M][n_kv/t][L][hd] bf16; err: the device error

@@ -133,3 +133,25 @@ def test_argument_errors_before_launch():
 def test_status_strings():
     for s in range(10):
         assert tpx.status_str(s).startswith("TP_")
+
+
+def test_attention_arguments_before_launch():
+    """Decode attention: workspace size from its definition (fp32 partials per 128-position chunk
+    and one counter per sequence and kv head), and the refusals that need no device."""
+    L_ = tpx.lib()
+    sh = tpx.make_shape(8192, n_q=64, n_kv=8, hd=128, t=8)
+    M, L, G = 32, 4096, 8
+    assert tpx.tp_attn_workspace_bytes(sh, M, L) == M * 8 * (L // 128) * G * (128 + 2) * 4 + M * 8 * 4
+    assert tpx.tp_attn_workspace_bytes(sh, 3, 130) == 3 * 8 * 2 * G * 130 * 4 + 3 * 8 * 4   # ragged chunk
+
+    def call(shape, M=4, L=256, ws_bytes=1 << 30, p=FAKE):
+        return L_.tp_attn_decode(ctypes.byref(shape), p, p, p, L, p, M, p, p, ws_bytes, None)
+
+    assert call(sh, M=-1) == tpx.TP_ERR_INVALID_ARG
+    assert call(sh, L=0) == tpx.TP_ERR_INVALID_ARG
+    assert call(tpx.make_shape(2176, n_q=34, n_kv=2, hd=64, t=2)) == tpx.TP_ERR_UNSUPPORTED   # 17 q per kv
+    assert call(tpx.make_shape(1536, n_q=16, n_kv=4, hd=96, t=2)) == tpx.TP_ERR_UNSUPPORTED   # head dim 96
+    assert call(sh, M=1 << 16, L=1 << 12) == tpx.TP_ERR_UNSUPPORTED                           # 2^31 cache rows
+    assert call(sh, ws_bytes=tpx.tp_attn_workspace_bytes(sh, 4, 256) - 1) == tpx.TP_ERR_WORKSPACE
+    assert call(sh, p=ctypes.c_void_p((1 << 20) + 8)) == tpx.TP_ERR_ALIGN
+    assert call(sh, M=0) == tpx.TP_OK

@@ -45,11 +45,11 @@ def run_case(dev, t, n_q, n_kv, hd, M, L, lens, seed=0, poison=False):
     qkv = inputs.normal_bf16((M, Q), 1.0, seed, 80, dev)
     kc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, seed, 81, dev)
     vc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, seed, 82, dev)
-    if poison:  # slots past each sequence's new token hold NaN: they must not reach the output
+    if poison:  # the new token's slot and every slot after it hold NaN before the call
         for m, n in enumerate(lens):
             if 0 <= n < L:
-                kc[:, m, :, n + 1:] = float("nan")
-                vc[:, m, :, n + 1:] = float("nan")
+                kc[:, m, :, n:] = float("nan")
+                vc[:, m, :, n:] = float("nan")
     k0, v0 = bits(kc).copy(), bits(vc).copy()
     lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
     o_in = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
@@ -76,7 +76,9 @@ def test_attention_small_shapes(dev, t, n_q, n_kv, hd):
 
 def test_attention_ignores_slots_past_the_length(dev):
     """Cache slots after the new token are never read into the result, even when they hold NaN
-    (a chunk is staged whole; its rows past the end must weigh exactly zero)."""
+    (a chunk is staged whole; its rows past the end must weigh exactly zero), and the new
+    token's own slot counts with the appended values even if it is staged before the append
+    lands (its old content here is NaN)."""
     lens = [5, 130, 299, 127]
     o_in, o_ref, _ = run_case(dev, 2, 8, 4, 128, 4, 300, lens, seed=3, poison=True)
     got = O.as_f64(bits(o_in))
