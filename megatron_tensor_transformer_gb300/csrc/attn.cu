@@ -65,7 +65,7 @@ struct ACfg {
   static constexpr int QSTR = HD * 2 + 16;  // padded q row (bytes): ldmatrix without conflicts
   static constexpr size_t kRing = (size_t)NS * STAGE;
   static constexpr size_t kQ = 16 * QSTR;
-  static constexpr size_t kML = 2 * CW * 16 * 4;
+  static constexpr size_t kML = 2 * 2 * CW * 16 * 4;  // maxima and sums, two buffers
   static constexpr size_t SMEM = 1024 + kRing + kQ + kML + (2 * NS + 1) * 8;
   static_assert((size_t)CW * 16 * HD * 4 == (size_t)STAGE, "a stage holds the warps' [16][HD] fp32 states");
 };
@@ -231,9 +231,8 @@ __global__ void __launch_bounds__(ACfg<HD>::NT + 32, 1)
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = ring + C::kRing;                                   // [16][QSTR] bf16, rows >= G zero
-  float* mw = reinterpret_cast<float*>(sQ + C::kQ);                // [CW][16] warps' maxima
-  float* lw = mw + C::CW * 16;                                     // [CW][16] warps' sums
-  uint64_t* bars = reinterpret_cast<uint64_t*>(lw + C::CW * 16);   // full[NS], empty[NS], consumers
+  float* mlw = reinterpret_cast<float*>(sQ + C::kQ);               // [2][2][CW][16] warps' maxima, sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mlw + 4 * C::CW * 16);  // full[NS], empty[NS], consumers
   constexpr int kMaxPieces = 32;
   __shared__ int s_last, s_npc, s_pc[kMaxPieces];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -344,6 +343,7 @@ __global__ void __launch_bounds__(ACfg<HD>::NT + 32, 1)
   int c_seg = cu.c;                                          // first chunk of the current piece
   // pieces of a split (sequence, kv head) this CTA leaves: only its first and last can be such
   int np_mine = 0, pm[2] = {0, 0}, pgg[2] = {0, 0}, pnch[2] = {0, 0};
+  int sb = 0;  // which max / sum buffer the next piece end uses
   long long pub[2] = {0, 0};
   for (int k = 0; k < nu; ++k) {
     const int st = k % C::NS;
@@ -459,26 +459,25 @@ __global__ void __launch_bounds__(ACfg<HD>::NT + 32, 1)
         l0 += __shfl_xor_sync(kFull, l0, o);
         l1 += __shfl_xor_sync(kFull, l1, o);
       }
+      // two buffers: a warp may reach the next piece end while another still reads these
+      float* mw = mlw + sb * 2 * C::CW * 16;
+      float* lw = mw + C::CW * 16;
+      sb ^= 1;
       if (qq == 0) {
         mw[warp * 16 + gq] = m0;
         mw[warp * 16 + gq + 8] = m1;
         lw[warp * 16 + gq] = l0;
         lw[warp * 16 + gq + 8] = l1;
       }
-      if (!csync()) return;  // every warp is past this chunk's reads of the stage and of sQ
-      float M0 = mw[gq], M1 = mw[gq + 8];
-#pragma unroll
-      for (int w = 1; w < C::CW; ++w) {
-        M0 = fmaxf(M0, mw[w * 16 + gq]);
-        M1 = fmaxf(M1, mw[w * 16 + gq + 8]);
-      }
-      const float f0 = __expf(m0 - M0), f1 = __expf(m1 - M1);  // 0 for a warp with no valid position
+      // every warp is past this chunk's reads of the stage and of sQ once all have arrived
+      // below; the raw p.v goes to the stage first (the warps' factors are applied when summing)
+      if (!csync()) return;
       float* wred = reinterpret_cast<float*>(stage) + (size_t)warp * 16 * HD;
 #pragma unroll
       for (int t8 = 0; t8 < HD / 8; ++t8) {  // row r at r * HD, its 8-float groups permuted by r & 7
-        const int d0 = (8 * t8) ^ ((gq & 7) << 3), d1 = (8 * t8) ^ (((gq + 8) & 7) << 3);
-        *reinterpret_cast<float2*>(wred + gq * HD + d0 + 2 * qq) = make_float2(O[t8][0] * f0, O[t8][1] * f0);
-        *reinterpret_cast<float2*>(wred + (gq + 8) * HD + d1 + 2 * qq) = make_float2(O[t8][2] * f1, O[t8][3] * f1);
+        const int d0 = (8 * t8) ^ ((gq & 7) << 3);
+        *reinterpret_cast<float2*>(wred + gq * HD + d0 + 2 * qq) = make_float2(O[t8][0], O[t8][1]);
+        *reinterpret_cast<float2*>(wred + (gq + 8) * HD + d0 + 2 * qq) = make_float2(O[t8][2], O[t8][3]);
       }
       if (!last) store_q();  // the next piece's q (sQ is free: every warp is past the csync above)
       if (!csync()) return;
@@ -487,19 +486,20 @@ __global__ void __launch_bounds__(ACfg<HD>::NT + 32, 1)
       __nv_bfloat16* out = o_in + (size_t)cu.m * g.n_q * HD + (size_t)(sh * g.nqs + gl * g.G) * HD;
       const bool whole = c_seg == 0 && cu.c + 1 == cu.nch;
       float* part = whole ? nullptr : part_ptr(g, ws, cu.m, cu.gg, c_seg);
-      for (int e = tid; e < g.G * HD; e += C::NT) {
+      for (int e = tid; e < g.G * HD; e += C::NT) {  // the warps' p.v, scaled to the common max, warp order
         const int hi = e / HD, d = e % HD, ds = d ^ ((hi & 7) << 3);
-        float v = red[hi * HD + ds];
+        float Mx = mw[hi];
 #pragma unroll
-        for (int w = 1; w < C::CW; ++w) v += red[((size_t)w * 16 + hi) * HD + ds];
-        if (whole) {
-          float Mx = mw[hi], Lx = 0.f;
-          for (int w = 1; w < C::CW; ++w) Mx = fmaxf(Mx, mw[w * 16 + hi]);
-          for (int w = 0; w < C::CW; ++w) Lx += lw[w * 16 + hi] * __expf(mw[w * 16 + hi] - Mx);
-          out[e] = __float2bfloat16_rn(v / Lx);
-        } else {
-          part[e] = v;
+        for (int w = 1; w < C::CW; ++w) Mx = fmaxf(Mx, mw[w * 16 + hi]);
+        float v = 0.f, Lx = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::CW; ++w) {
+          const float f = __expf(mw[w * 16 + hi] - Mx);  // 0 for a warp with no valid position
+          v += red[((size_t)w * 16 + hi) * HD + ds] * f;
+          Lx += lw[w * 16 + hi] * f;
         }
+        if (whole) out[e] = __float2bfloat16_rn(v / Lx);
+        else part[e] = v;
       }
       if (!whole && tid < g.G) {
         float Mx = mw[tid], Lx = 0.f;
@@ -515,8 +515,9 @@ __global__ void __launch_bounds__(ACfg<HD>::NT + 32, 1)
         pub[np_mine] = u0 + k - cu.c;  // unit of chunk 0 of (m, gg)
         ++np_mine;
       }
-      fence_proxy_async_smem();  // the generic writes above, before the producer's next copy here
-      if (!csync()) return;      // the stage, mw and lw are free again
+      // The stage returns to the producer once every warp has arrived below, each after its
+      // own reads of it; the generic writes to it are ordered before the next copy.
+      fence_proxy_async_smem();
 #pragma unroll
       for (int t8 = 0; t8 < HD / 8; ++t8) O[t8][0] = O[t8][1] = O[t8][2] = O[t8][3] = 0.f;
       m0 = m1 = -INFINITY;
