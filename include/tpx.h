@@ -114,7 +114,10 @@ typedef struct {
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernels (rows % 128, K % 64); default:
                                      tcgen05 where supported, except e4m3 weights at decode token counts
-                                     (M <= 64), which stream faster through the mma.sync kernel */
+                                     (M <= 64).  Those go to the TMA-fed mma.sync kernel (M <= 32, 128-row
+                                     tiles, k % 128, a workspace given; widening in registers, work split
+                                     evenly over two CTAs per SM, fused and unfused folds give the same
+                                     bits), else to the register-direct mma.sync kernel */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, bf16 weights, 128-row
                                      and 64-k tiles) runs as ONE persistent launch: the column-parallel

@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "fused.h"
 #include "pack.h"
+#include "ring.h"
 #include "skinny.h"
 #include "small.h"
 #include "tc.h"
@@ -256,8 +257,8 @@ bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
   if (!tc_supported(rows, K, fp8)) return false;
   if (flags & TP_F_KERNEL_TC) return true;
-  // e4m3 decode: the mma.sync kernel, which widens in registers, streams faster (measured:
-  // 70B MLP block at M = 16, 4.23 vs 3.47 TB/s for the tcgen05 path)
+  // e4m3 decode: the mma.sync kernels, which widen in registers, stream faster (measured, 70B
+  // layer at M = 16: 215 us TMA-fed, 236 us register-direct, 292 us for the tcgen05 path)
   if (fp8 && M <= kFusedMaxM) return false;
   return M > kTcMinM;
 }
@@ -284,6 +285,36 @@ void set_streamk(TcArgs& a, void* sk_ws) {
   a.pieces = static_cast<float*>(sk_ws);
   a.item_tickets = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(sk_ws) + tc_streamk_bytes() -
                                                (size_t)kTcMaxStreamkItems * 4);
+}
+
+// The TMA-fed e4m3 decode kernel: e4m3 weights, 1..32 tokens, 128-row tiles, unless the
+// mma.sync kernel is asked for, and only with a workspace (its piece slots go in the stream-K
+// scratch, its counters in the zero-between-calls ticket words that follow it).
+bool pick_ring(uint32_t flags, const tp_packed_desc* d, int rows, int K, int M, bool rowpar, const void* ws,
+               size_t ws_bytes) {
+  if (d->wtype != TP_FP8_E4M3 || (flags & TP_F_KERNEL_SKINNY) || !ws || d->shape.t > 8) return false;
+  if (!ring_supported(rows, K, M, d->shape.t)) return false;
+  if (ring_pieces_bytes(M) > sk_bytes()) return false;
+  if (ring_counter_words(rows, d->shape.t, rowpar) * 4 > ticket_bytes(rowpar ? rows : d->shape.d)) return false;
+  return ws_bytes >= sk_bytes() + ticket_bytes(rowpar ? rows : d->shape.d) && aligned16(ws);
+}
+
+RingArgs ring_args(const tp_packed_desc* d, const void* w, int rows, int K, const bf16* x, int ldx, int M,
+                   void* ws) {
+  RingArgs r{};
+  r.w = static_cast<const uint8_t*>(w);
+  r.shard_stride = d->shard_stride_bytes;
+  r.scales_offset = d->scales_offset;
+  r.rows = rows;
+  r.K = K;
+  r.t = d->shape.t;
+  r.x = x;
+  r.ldx = ldx;
+  r.M = M;
+  r.pieces = static_cast<float*>(ws);
+  r.counters = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + sk_bytes());
+  r.err = tc_error_word();
+  return r;
 }
 
 // Weights of a tcgen05 launch.  e4m3 weights stream as they are (widened in shared memory by
@@ -340,6 +371,16 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     set_streamk(a, sk_ws);
     return launch_tc(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
   }
+  if ((mode == COLPAR_BF16 || mode == COLPAR_SWIGLU) &&
+      pick_ring(flags, d, rows, K, M, false, sk_ws, ws_bytes)) {
+    RingArgs r = ring_args(d, w, rows, K, x, K, M, sk_ws);
+    if (!r.err) return TP_ERR_CUDA;
+    r.rowpar = 0;
+    r.mode = mode;
+    r.out = out;
+    r.ldo = ldo;
+    return launch_ring(r, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
     ColparArgs a{};
     a.w = static_cast<const uint8_t*>(w);
@@ -371,7 +412,8 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   if (plan.R == 0) return TP_ERR_ALIGN;
   const bool unfused = (flags & TP_F_UNFUSED_REDUCE) != 0;
   const bool tc = pick_tc(flags, N, K, d->wtype == TP_FP8_E4M3, M);
-  const bool need_ws = !partials_user && (unfused || plan.S > 1 || tc);
+  const bool ring = !tc && pick_ring(flags, d, N, K, M, true, ws, ws_bytes);
+  const bool need_ws = !partials_user && (unfused || plan.S > 1 || tc || ring);
   float* wsP = nullptr;
   unsigned* tickets = nullptr;
   void* sk_ws = nullptr;
@@ -423,6 +465,20 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       if (launch_tc(a, st, pdl) != cudaSuccess) return TP_ERR_CUDA;
       if (launch_reduce(wsP, t, mb, N, a.residual, a.y, st) != cudaSuccess) return TP_ERR_CUDA;
     }
+    return TP_OK;
+  }
+  if (ring) {
+    RingArgs r = ring_args(d, w, N, K, a_in, K * t, M, ws);
+    if (!r.err) return TP_ERR_CUDA;
+    r.rowpar = 1;
+    r.residual = res;
+    r.y = y;
+    r.ldy = N;
+    r.partials = partials_user ? partials_user : wsP;
+    r.pM = M;
+    r.mode = (partials_user || unfused) ? FOLD_NONE : FOLD_TICKET;
+    if (launch_ring(r, st, (flags & TP_F_SERIAL) == 0) != cudaSuccess) return TP_ERR_CUDA;
+    if (!partials_user && unfused && launch_reduce(wsP, t, M, N, res, y, st) != cudaSuccess) return TP_ERR_CUDA;
     return TP_OK;
   }
   for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {
