@@ -540,9 +540,10 @@ def run_lm_head(args, rank, world, local):
 
 def run_attn(args, rank, world, local):
     """Llama-3.1 70B attention block with a real KV cache: 32 sequences, each with 4095 cached
-    positions (4096 with the new token), t=8.  One step = QKV (column-parallel) + the
-    head-sharded decode attention over the cache + o_proj (row-parallel, shard fold, residual).
-    The roofline kernel is the attention (cache reads: M x n_kv x 4096 x hd x 2 x 2 bytes)."""
+    positions (4096 with the new token), t=8.  One step = one tp_attn_block_forward: QKV
+    (column-parallel) + the head-sharded decode attention over the cache + o_proj (row-parallel,
+    shard fold, residual).  The roofline kernel is the attention (cache reads: M x n_kv x 4096 x
+    hd x 2 x 2 bytes)."""
     import torch
     from megatron_tensor_transformer_gb300 import inputs, tpx
 
@@ -561,14 +562,12 @@ def run_attn(args, rank, world, local):
     qkv = torch.empty((M, (n_q + 2 * n_kv) * hd), dtype=torch.bfloat16, device=dev)
     o_in = torch.empty((M, n_q * hd), dtype=torch.bfloat16, device=dev)
     y = torch.empty_like(x)
-    ws = tpx.new_workspace(sh, M, dev)
+    bws = tpx.new_attn_block_workspace(sh, M, L, dev)
     aws = torch.empty(tpx.tp_attn_workspace_bytes(sh, M, L), dtype=torch.uint8, device=dev)
     K = args.steps
 
     def step():
-        tpx.tp_colpar_forward(q, q_w, x, qkv, ws=ws, stream=stream)
-        tpx.tp_attn_decode(sh, qkv, kc, vc, lens, o_in, aws, stream=stream)
-        tpx.tp_rowpar_forward(o, o_w, o_in, x, y, ws, stream=stream)
+        tpx.tp_attn_block_forward(q, q_w, o, o_w, x, x, kc, vc, lens, y, qkv, o_in, bws, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):

@@ -254,6 +254,24 @@ size_t tp_attn_workspace_bytes(const tp_shape* shape /* host */, int32_t M, int3
 tp_status tp_attn_decode(const tp_shape* shape /* host */, const void* qkv, void* k_cache, void* v_cache, int32_t L,
                          const int32_t* lens, int32_t M, void* o_in, void* ws, size_t ws_bytes, void* stream);
 
+/* The attention block of a decode step over a KV cache ("TPAttentionBlock" with a real
+ * attention core, scalablesystem.dev "The Tensor-Parallel Shard Group"), in one call:
+ *   qkv_out = x . Wqkv                       column-parallel, shard-major (tp_colpar_forward)
+ *   cache[lens[m]] = the new k, v;  o_in = attention over positions 0..lens[m] (tp_attn_decode)
+ *   y = residual + o_in . Wo                 row-parallel, shards folded in order (tp_rowpar_forward)
+ * qkv, o: QKV and O descriptors of one block; x, residual (nullable), y: [M, d] bf16 (y must not
+ * alias x or residual); k_cache, v_cache, L, lens as for tp_attn_decode; qkv_out [M, (n_q+2n_kv)hd]
+ * and o_in [M, n_q hd]: caller's bf16 buffers that keep the step's q, k, v and attention output.
+ * ws: tp_attn_block_workspace_bytes(shape, M, L, flags) bytes, zero-filled once before first use
+ * (its head is the projections' workspace, its tail the attention's).  Errors as for the three
+ * calls; four kernel launches for bf16 weights at decode token counts. */
+size_t tp_attn_block_workspace_bytes(const tp_shape* shape /* host */, int32_t M, int32_t L, uint32_t flags);
+tp_status tp_attn_block_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
+                                const tp_packed_desc* o /* host */, const void* o_w, const void* x,
+                                const void* residual, int32_t M, void* k_cache, void* v_cache, int32_t L,
+                                const int32_t* lens, void* y, void* qkv_out, void* o_in, void* ws,
+                                size_t ws_bytes, uint32_t flags, void* stream);
+
 /* Vocabulary-parallel lm_head (the column-parallel GEMM at the model's output edge; each shard's
  * logits are a slice of the output, so the pages' all-gather is a concatenation, scalablesystem.dev
  * "The Tensor-Parallel Shard Group"): logits[m][v] = sum_k x[m][k] W[k][v] for v < vocab, fp32

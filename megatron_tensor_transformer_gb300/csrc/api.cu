@@ -800,6 +800,49 @@ tp_status tp_attn_decode(const tp_shape* sh, const void* qkv, void* k_cache, voi
                                         static_cast<float*>(ws), err, S(stream)));
 }
 
+size_t tp_attn_block_workspace_bytes(const tp_shape* sh, int32_t M, int32_t L, uint32_t flags) {
+  if (!sh || M < 0 || L <= 0) return 0;
+  const size_t proj = tp_workspace_bytes(sh, M, flags), attn = tp_attn_workspace_bytes(sh, M, L);
+  if (proj == 0 || attn == 0) return 0;
+  return (size_t)align_up(proj) + attn;
+}
+
+tp_status tp_attn_block_forward(const tp_packed_desc* qkv, const void* qkv_w, const tp_packed_desc* o,
+                                const void* o_w, const void* x, const void* residual, int32_t M, void* k_cache,
+                                void* v_cache, int32_t L, const int32_t* lens, void* y, void* qkv_out, void* o_in,
+                                void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
+  tp_status st = check_desc(qkv, TP_W_QKV, qkv_w);
+  if (st != TP_OK) return st;
+  st = check_desc(o, TP_W_O, o_w);
+  if (st != TP_OK) return st;
+  if (!same_block(qkv->shape, o->shape, false)) return TP_ERR_LAYOUT_MISMATCH;
+  if ((flags & ~kFwdFlags) || bad_kernel_flags(flags)) return TP_ERR_INVALID_ARG;
+  const tp_shape& sh = qkv->shape;
+  if (M < 0 || L <= 0) return TP_ERR_INVALID_ARG;
+  if (!attn_supported(sh.head_dim, sh.n_q_heads / sh.n_kv_heads)) return TP_ERR_UNSUPPORTED;
+  if ((int64_t)M * sh.n_kv_heads * L >= (int64_t(1) << 31)) return TP_ERR_UNSUPPORTED;
+  if (M == 0) return TP_OK;
+  if (!x || !y || !qkv_out || !o_in || !k_cache || !v_cache || !lens) return TP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(qkv_out) || !aligned16(o_in) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || (residual && !aligned16(residual)))
+    return TP_ERR_ALIGN;
+  const size_t proj = align_up(tp_workspace_bytes(&sh, M, flags));
+  if (!ws || ws_bytes < tp_attn_block_workspace_bytes(&sh, M, L, flags)) return TP_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TP_ERR_ALIGN;
+  unsigned* err = tc_error_word();
+  if (!err) return TP_ERR_CUDA;
+  cudaStream_t s = S(stream);
+  st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qkv_out, COLPAR_BF16, s, flags, ws, proj);
+  if (st != TP_OK) return st;
+  st = cuda_status(launch_attn_decode(sh.t, M, L, sh.n_q_heads, sh.n_kv_heads, sh.head_dim,
+                                      static_cast<const bf16*>(qkv_out), static_cast<bf16*>(k_cache),
+                                      static_cast<bf16*>(v_cache), lens, static_cast<bf16*>(o_in),
+                                      reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + proj), err, s));
+  if (st != TP_OK) return st;
+  return run_rowpar(o, o_w, static_cast<const bf16*>(o_in), M, static_cast<const bf16*>(residual),
+                    static_cast<bf16*>(y), nullptr, ws, proj, flags, s);
+}
+
 tp_status tp_lm_head_forward(const tp_packed_desc* desc, const void* w, const void* x, int32_t M, float* logits,
                              void* ws, size_t ws_bytes, uint32_t flags, void* stream) {
   tp_status st = check_desc(desc, TP_W_VOCAB, w);

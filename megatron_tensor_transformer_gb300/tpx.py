@@ -24,7 +24,8 @@ EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspa
            "tp_rowpar_partials", "tp_rowpar_forward", "tp_rowpar_forward_noalloc",
            "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
            "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count",
-           "tp_lm_head_forward", "tp_embed_lookup", "tp_attn_workspace_bytes", "tp_attn_decode"]
+           "tp_lm_head_forward", "tp_embed_lookup", "tp_attn_workspace_bytes", "tp_attn_decode",
+           "tp_attn_block_workspace_bytes", "tp_attn_block_forward"]
 
 
 class TpxError(RuntimeError):
@@ -83,6 +84,9 @@ def lib():
             "tp_embed_lookup": (I32, [P(PackedDesc), V, V, I32, V, V]),
             "tp_attn_workspace_bytes": (SZ, [P(Shape), I32, I32]),
             "tp_attn_decode": (I32, [P(Shape), V, V, V, I32, V, I32, V, V, SZ, V]),
+            "tp_attn_block_workspace_bytes": (SZ, [P(Shape), I32, I32, U32]),
+            "tp_attn_block_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, V, V, I32, V, V, I32, V, V, V, V,
+                                            V, SZ, U32, V]),
             "tp_launch_count": (ctypes.c_uint64, []),
         }
         for name, (res, args) in sig.items():
@@ -251,6 +255,26 @@ def tp_embed_lookup(desc, w, ids, x, stream=None):
     _check(lib().tp_embed_lookup(ctypes.byref(desc), _ptr(w), _ptr(ids), ids.shape[0], _ptr(x), _stream(stream)),
            "tp_embed_lookup")
     return x
+
+
+def tp_attn_block_workspace_bytes(shape, M, L, flags=0):
+    return lib().tp_attn_block_workspace_bytes(ctypes.byref(shape), M, L, flags)
+
+
+def new_attn_block_workspace(shape, M, L, device, flags=0):
+    """Zero-filled workspace of tp_attn_block_forward (its projection counters start at zero)."""
+    return torch.zeros(max(1, tp_attn_block_workspace_bytes(shape, M, L, flags)), dtype=torch.uint8, device=device)
+
+
+def tp_attn_block_forward(qkv, qkv_w, o, o_w, x, residual, k_cache, v_cache, lens, y, qkv_out, o_in, ws, flags=0,
+                          stream=None):
+    """k_cache, v_cache: [t, M, n_kv/t, L, hd] bf16; lens: [M] int32 on the device."""
+    L = k_cache.shape[3]
+    _check(lib().tp_attn_block_forward(ctypes.byref(qkv), _ptr(qkv_w), ctypes.byref(o), _ptr(o_w), _ptr(x),
+                                       _ptr(residual), x.shape[0], _ptr(k_cache), _ptr(v_cache), L, _ptr(lens),
+                                       _ptr(y), _ptr(qkv_out), _ptr(o_in), _ptr(ws), ws.numel(), flags,
+                                       _stream(stream)), "tp_attn_block_forward")
+    return y
 
 
 def tp_attn_workspace_bytes(shape, M, L):

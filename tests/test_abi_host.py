@@ -155,3 +155,32 @@ def test_attention_arguments_before_launch():
     assert call(sh, ws_bytes=tpx.tp_attn_workspace_bytes(sh, 4, 256) - 1) == tpx.TP_ERR_WORKSPACE
     assert call(sh, p=ctypes.c_void_p((1 << 20) + 8)) == tpx.TP_ERR_ALIGN
     assert call(sh, M=0) == tpx.TP_OK
+
+
+def test_attention_block_arguments_before_launch():
+    """The one-call attention block: its workspace is the projections' (aligned) then the
+    attention's; shape, workspace and flag refusals need no device."""
+    L_ = tpx.lib()
+    sh = tpx.make_shape(8192, n_q=64, n_kv=8, hd=128, t=8)
+    M, L = 32, 4096
+    proj = tpx.tp_workspace_bytes(sh, M)
+    need = -(-proj // 256) * 256 + tpx.tp_attn_workspace_bytes(sh, M, L)
+    assert tpx.tp_attn_block_workspace_bytes(sh, M, L) == need
+    q, o = tpx.tp_describe(sh, tpx.TP_W_QKV), tpx.tp_describe(sh, tpx.TP_W_O)
+
+    def call(qd=q, od=o, M=4, L=256, ws_bytes=1 << 32, flags=0, p=FAKE):
+        return L_.tp_attn_block_forward(ctypes.byref(qd), FAKE, ctypes.byref(od), FAKE, p, None, M, p, p, L, p,
+                                        p, p, p, p, ws_bytes, flags, None)
+
+    assert call(M=-1) == tpx.TP_ERR_INVALID_ARG
+    assert call(L=0) == tpx.TP_ERR_INVALID_ARG
+    assert call(flags=0x100) == tpx.TP_ERR_INVALID_ARG
+    assert call(ws_bytes=tpx.tp_attn_block_workspace_bytes(sh, 4, 256) - 1) == tpx.TP_ERR_WORKSPACE
+    assert call(p=ctypes.c_void_p((1 << 20) + 8)) == tpx.TP_ERR_ALIGN
+    assert call(od=q) == tpx.TP_ERR_LAYOUT_MISMATCH                       # O slot given a QKV descriptor
+    o4 = tpx.tp_describe(tpx.make_shape(8192, n_q=64, n_kv=8, hd=128, t=4), tpx.TP_W_O)
+    assert call(od=o4) == tpx.TP_ERR_LAYOUT_MISMATCH                      # the two halves of different blocks
+    sh17 = tpx.make_shape(2176, n_q=34, n_kv=2, hd=64, t=2)
+    assert call(qd=tpx.tp_describe(sh17, tpx.TP_W_QKV), od=tpx.tp_describe(sh17, tpx.TP_W_O)) == \
+        tpx.TP_ERR_UNSUPPORTED                                            # 17 q heads per kv head
+    assert call(M=0) == tpx.TP_OK

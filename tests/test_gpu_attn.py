@@ -126,3 +126,52 @@ def test_attention_block_end_to_end(dev):
     o_ref = O.f64_to_bf16_bits(O.attention_decode(qkv_ref, k_ref, v_ref, lens, n_q, n_kv, hd))
     y_ref = O.as_f64(o_ref) @ O.as_f64(bits(wo)) + O.as_f64(bits(x))
     check_close(bits(y), y_ref, what="attention block with a KV cache")
+
+
+@pytest.mark.parametrize("wtype", [tpx.TP_BF16, tpx.TP_FP8_E4M3])
+def test_attention_block_in_one_call(dev, wtype):
+    """tp_attn_block_forward = QKV, the cache append + attention, o_proj with the shard fold, in one
+    call: the same bits as the three calls, and the oracle's block within the bars (for e4m3
+    weights, the oracle on the dequantised weights)."""
+    d, n_q, n_kv, hd, t, M, L = 2048, 16, 8, 128, 8, 4, 1024
+    x, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, M, seed=5, device=dev)
+    sh = tpx.make_shape(d, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=wtype)
+    q_w, q = tpx.tp_partition_weights(sh, tpx.TP_W_QKV, wqkv)
+    o_w, o = tpx.tp_partition_weights(sh, tpx.TP_W_O, wo)
+    kc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, 5, 85, dev)
+    vc = inputs.normal_bf16((t, M, n_kv // t, L, hd), 1.0, 5, 86, dev)
+    k0, v0 = bits(kc).copy(), bits(vc).copy()
+    kc2, vc2 = kc.clone(), vc.clone()
+    lens = [1023, 0, 300, 777]
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    Q = (n_q + 2 * n_kv) * hd
+    # one call
+    qkv1 = torch.full((M, Q), float("nan"), dtype=torch.bfloat16, device=dev)
+    o1 = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
+    y1 = torch.full_like(x, float("nan"))
+    bws = tpx.new_attn_block_workspace(sh, M, L, dev)
+    tpx.tp_attn_block_forward(q, q_w, o, o_w, x, x, kc, vc, lens_d, y1, qkv1, o1, bws)
+    # three calls
+    qkv2 = torch.empty((M, Q), dtype=torch.bfloat16, device=dev)
+    o2 = torch.empty((M, n_q * hd), dtype=torch.bfloat16, device=dev)
+    y2 = torch.empty_like(x)
+    ws = tpx.new_workspace(sh, M, dev)
+    aws = torch.empty(tpx.tp_attn_workspace_bytes(sh, M, L), dtype=torch.uint8, device=dev)
+    tpx.tp_colpar_forward(q, q_w, x, qkv2, ws=ws)
+    tpx.tp_attn_decode(sh, qkv2, kc2, vc2, lens_d, o2, aws)
+    tpx.tp_rowpar_forward(o, o_w, o2, x, y2, ws)
+    assert tpx.tp_sync(timeout_ms=20000) == tpx.TP_OK
+    for a_, b_ in ((qkv1, qkv2), (o1, o2), (y1, y2), (kc, kc2), (vc, vc2)):
+        assert torch.equal(a_.view(torch.int16), b_.view(torch.int16))
+    # oracle
+    wq_ref, wo_ref = O.as_f64(bits(wqkv)), O.as_f64(bits(wo))
+    if wtype == tpx.TP_FP8_E4M3:
+        wq_ref = O.dequantize_fp8(*O.quantize_fp8_per_channel(wq_ref))
+        wo_ref = O.dequantize_fp8(*O.quantize_fp8_per_channel(wo_ref))
+    qkv_ref = O.f64_to_bf16_bits(O.as_f64(bits(x)) @ wq_ref)
+    cols = np.concatenate([O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0] for s in range(t)])
+    check_close(bits(qkv1), O.as_f64(qkv_ref)[:, cols], what="block qkv")
+    k_ref, v_ref = O.append_kv(qkv_ref, cache_to_oracle(k0, t), cache_to_oracle(v0, t), lens, n_q, n_kv, hd)
+    o_ref = O.f64_to_bf16_bits(O.attention_decode(qkv_ref, k_ref, v_ref, lens, n_q, n_kv, hd))
+    y_ref = O.as_f64(o_ref) @ wo_ref + O.as_f64(bits(x))
+    check_close(bits(y1), y_ref, what=f"attention block in one call, wtype {wtype}")
