@@ -14,8 +14,8 @@ What it computes, in float64, following the pages:
     shard's heads, o_proj row-parallel with one sum.
   * The shard layouts (column split = output dim, row split = input dim).
   * FP8 e4m3 per-output-channel weight quantization (the pages' "FP8"
-    replica-density mode) and the bf16 / e4m3 number formats from their
-    bit definitions.
+    replica-density mode), per-token activation quantization for the FP8 x FP8
+    path, and the bf16 / e4m3 number formats from their bit definitions.
   * The byte and flop accounting the pages print.
 
 Everything is the plain definition: no blocking, fusion or reordering.  The
@@ -278,6 +278,45 @@ def quantize_fp8_per_channel(w):
 def dequantize_fp8(q, s):
     """W_deq[k,n] = e4m3(q[k,n]) * s_n, in float64."""
     return e4m3_bits_to_f64(q) * np.asarray(s, dtype=np.float64)[None, :]
+
+
+# --------------------------------------------------------------------------
+# FP8 x FP8: activations quantised per token as well ("FP8" prefill, vidyal.ai
+# model-parallelism, which credits FP8 with up to 50% higher prefill).  The pages give
+# no activation scale; the reading here mirrors their weight scheme with one scale
+# per token (row) over the whole, unsharded row.
+# --------------------------------------------------------------------------
+
+
+def quantize_fp8_per_token(x):
+    """X [M,K] -> (q bits [M,K] uint8, s [M] float32) with X ~ diag(s) q.
+    s_m = absmax_k |X[m,k]| / 448 in binary32 (an all-zero row gets s_m = 1);
+    q = E4M3_RNE_satfinite(X / s_m), the division in binary32."""
+    x32 = as_f64(x).astype(np.float32)
+    amax = np.max(np.abs(x32), axis=1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = f32_to_e4m3_bits_satfinite(x32 / s[:, None])
+    return q, s
+
+
+def dequantize_fp8_per_token(q, s):
+    """X_deq[m,k] = e4m3(q[m,k]) * s_m, in float64."""
+    return e4m3_bits_to_f64(q) * np.asarray(s, dtype=np.float64)[:, None]
+
+
+def mlp_fp8x(x, w_gate, w_up, w_down, residual=None):
+    """The MLP with both GEMM inputs quantised per token (weights as given, normally the
+    dequantised per-channel e4m3 weights):
+        a = Q(x);  h = bf16(silu(a Wg) * (a Wu));  y = residual + Q(h) Wd
+    Q = quantize_fp8_per_token then dequantise.  h is rounded to bf16 first, because the
+    quantiser of the row-parallel input sees the stored bf16 activations.  x holds bf16
+    values.  Returns (y, h) in float64 (h on the bf16 grid)."""
+    a = dequantize_fp8_per_token(*quantize_fp8_per_token(x))
+    h = bf16_bits_to_f64(f64_to_bf16_bits(silu(a @ as_f64(w_gate)) * (a @ as_f64(w_up))))
+    y = dequantize_fp8_per_token(*quantize_fp8_per_token(h)) @ as_f64(w_down)
+    if residual is not None:
+        y = y + as_f64(residual)
+    return y, h
 
 
 # --------------------------------------------------------------------------

@@ -439,3 +439,78 @@ def test_attention_head_sharded_equals_unsharded(t):
         o_s = O.attention_decode(qkv_s, k2[:, s * nkvs:(s + 1) * nkvs], v2[:, s * nkvs:(s + 1) * nkvs], lens,
                                  nqs, nkvs, hd)
         np.testing.assert_allclose(o_s, full[:, s * nqs * hd:(s + 1) * nqs * hd], rtol=0, atol=0)
+
+
+# ---------------------------------------------------------------- FP8 x FP8: per-token activations
+
+
+def test_fp8_per_token_quantizer_properties():
+    rng = np.random.default_rng(11)
+    x = (rng.normal(size=(40, 64)) * 3.0).astype(np.float32)
+    x[5, :] = 0.0
+    q, s = O.quantize_fp8_per_token(x)
+    assert s[5] == 1.0 and np.all(q[5] == 0)
+    amax_cols = np.argmax(np.abs(x), axis=1)
+    for m in range(40):
+        if m != 5:
+            assert q[m, amax_cols[m]] & 0x7F == 0x7E          # each row's absmax lands on +-448
+    deq = O.dequantize_fp8_per_token(q, s)
+    err = np.abs(deq - x.astype(np.float64))
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, s[:, None].astype(np.float64) * 2.0 ** -10) * (1 + 1e-6)
+    assert np.all(err <= bound)
+    # rows are independent: scaling one row leaves the others' codes alone
+    x2 = x.copy()
+    x2[0] *= 1000.0
+    q2, _ = O.quantize_fp8_per_token(x2)
+    assert np.array_equal(q2[1:], q[1:])
+
+
+def test_fp8_per_token_is_the_per_channel_quantizer_of_the_transpose():
+    rng = np.random.default_rng(12)
+    x = (rng.normal(size=(17, 33)) * 0.7).astype(np.float32)
+    q, s = O.quantize_fp8_per_token(x)
+    qt, st = O.quantize_fp8_per_channel(x.T)
+    assert np.array_equal(q, qt.T) and np.array_equal(s, st)
+
+
+def test_fp8_per_token_exact_values_round_trip():
+    vals = np.array([448, 1, -0.5, 0.015625, 2 ** -9, 96, -448, 0], dtype=np.float32)
+    x = np.stack([vals * 2.0 ** -10, vals, vals * 2.0 ** 6], axis=0).astype(np.float32)
+    q, s = O.quantize_fp8_per_token(x)
+    assert np.array_equal(O.dequantize_fp8_per_token(q, s), x.astype(np.float64))
+
+
+def _quant_row_loops(row):
+    """Per-token quantisation of one row with plain loops (binary32 as numpy scalars)."""
+    amax = np.float32(0.0)
+    for v in row:
+        amax = max(amax, abs(np.float32(v)))
+    s = amax / np.float32(448.0) if amax > 0 else np.float32(1.0)
+    return [O.e4m3_bits_to_f64(O.f32_to_e4m3_bits_satfinite(np.array([np.float32(v) / s], dtype=np.float32)))[0]
+            * float(s) for v in row]
+
+
+def test_mlp_fp8x_brute_force_and_special_cases():
+    rng = np.random.default_rng(13)
+    M, d, F = 3, 8, 6
+    x = O.bf16_bits_to_f64(O.f64_to_bf16_bits(rng.normal(size=(M, d))))
+    wg, wu, wd = (rng.normal(size=sh) * 0.5 for sh in ((d, F), (d, F), (F, d)))
+    y, h = O.mlp_fp8x(x, wg, wu, wd, residual=x)
+    for m in range(M):
+        a = _quant_row_loops(x[m])
+        hm = []
+        for f in range(F):
+            g = sum(a[k] * wg[k, f] for k in range(d))
+            u = sum(a[k] * wu[k, f] for k in range(d))
+            hm.append(float(O.bf16_bits_to_f64(O.f64_to_bf16_bits(np.array([g / (1 + np.exp(-g)) * u])))[0]))
+        assert np.allclose(h[m], hm, rtol=0, atol=0)
+        hq = _quant_row_loops(np.array(hm))
+        for n in range(d):
+            ref = sum(hq[f] * wd[f, n] for f in range(F)) + x[m, n]
+            assert abs(y[m, n] - ref) <= 1e-12 * (1 + abs(ref))
+    # rows already on a power-of-two-scaled e4m3 grid quantise exactly: the column-parallel half
+    # then equals the plain MLP's, rounded to bf16
+    xe = np.array([[448, 1, -0.5, 96, 0, 2 ** -9, -448, 0.015625]], dtype=np.float64) * 2.0 ** -6
+    _, h1 = O.mlp_fp8x(xe, wg, wu, wd)
+    _, h0 = O.mlp(xe, wg, wu, wd)
+    assert np.array_equal(h1, O.bf16_bits_to_f64(O.f64_to_bf16_bits(h0)))
