@@ -118,6 +118,14 @@ typedef struct {
                                      tiles, k % 128, a workspace given; widening in registers, work split
                                      evenly over two CTAs per SM, fused and unfused folds give the same
                                      bits), else to the register-direct mma.sync kernel */
+#define TP_F_FP8_ACT 0x200u       /* e4m3 weights: also quantise each GEMM's activations per token (s_m =
+                                     absmax/448 over the token's whole row, e4m3 RNE satfinite, as
+                                     tp_quantize_fp8_per_token) and multiply e4m3 x e4m3 on the tensor
+                                     cores, both scales applied to the fp32 result.  A different numeric
+                                     reading from the default (the pages give no activation scale), for
+                                     prefill: the tensor rate is twice bf16's.  tcgen05 kernels, rows %
+                                     128 and k % 128; the workspace grows by M x the widest activation row
+                                     (tp_workspace_bytes with this flag). */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, bf16 weights, 128-row
                                      and 64-k tiles) runs as ONE persistent launch: the column-parallel
@@ -286,6 +294,12 @@ tp_status tp_lm_head_forward(const tp_packed_desc* desc /* host */, const void* 
  * TP_W_EMBED buffer; ids: [M] int32 (device); x: [M, d] bf16.  M == 0 is a no-op. */
 tp_status tp_embed_lookup(const tp_packed_desc* desc /* host */, const void* w, const int32_t* ids, int32_t M,
                           void* x, void* stream);
+
+/* Per-token e4m3 quantisation of activations (the TP_F_FP8_ACT path's first step, exported for
+ * exact tests): x [M, K] bf16 (device, row stride K), s[m] = absmax_k |x[m][k]| / 448 in IEEE
+ * binary32 (1 for an all-zero row), q[m][k] = e4m3 RNE satfinite of x[m][k] / s[m] (binary32
+ * divide).  q: [M, K] bytes; s: [M] fp32 (device).  K % 8 == 0; pointers 16-byte aligned. */
+tp_status tp_quantize_fp8_per_token(const void* x, int32_t M, int32_t K, void* q, float* s, void* stream);
 
 /* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g). */
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,

@@ -130,6 +130,20 @@ uint64_t widen_bytes(const tp_shape* sh, int M) {
   return align_up(b);
 }
 
+// FP8 x FP8 (TP_F_FP8_ACT): the quantised activations of the widest GEMM input of the block
+// ([M][width] e4m3) and their per-token scales; it follows the widening scratch.
+uint64_t act_width(const tp_shape* sh) {
+  uint64_t w = (uint64_t)sh->d;
+  if (sh->ffn > 0 && (uint64_t)sh->ffn > w) w = (uint64_t)sh->ffn;
+  if (sh->n_q_heads > 0 && sh->head_dim > 0 && (uint64_t)sh->n_q_heads * sh->head_dim > w)
+    w = (uint64_t)sh->n_q_heads * sh->head_dim;
+  return w;
+}
+uint64_t act_bytes(const tp_shape* sh, int M, uint32_t flags) {
+  if (!(flags & TP_F_FP8_ACT) || sh->wtype != TP_FP8_E4M3 || M <= 0) return 0;
+  return align_up((uint64_t)M * act_width(sh)) + align_up((uint64_t)M * 4);
+}
+
 // RMSNorm scratch of the fused layer (per-tile sums of squares, two per-token factor arrays);
 // it follows the partials in the workspace.
 uint64_t norm_bytes(int d) { return align_up((uint64_t)fused_norm_words(d) * 4); }
@@ -144,6 +158,18 @@ void* widen_scratch(void* ws, size_t ws_bytes, const tp_shape& sh, int M, uint64
   const uint64_t off = sk_bytes() + ticket_bytes(sh.d) + partials_bytes(sh.t, M, sh.d) + norm_bytes(sh.d);
   if (ws_bytes < off + need) return nullptr;
   return static_cast<uint8_t*>(ws) + off;
+}
+
+// The FP8 x FP8 activation scratch of a workspace: codes, then scales; false if it does not fit.
+bool act_scratch(void* ws, size_t ws_bytes, const tp_shape& sh, int M, uint32_t flags, uint8_t*& q, float*& s) {
+  const uint64_t need = act_bytes(&sh, M, flags);
+  if (!ws || need == 0) return false;
+  const uint64_t off = sk_bytes() + ticket_bytes(sh.d) + partials_bytes(sh.t, M, sh.d) + norm_bytes(sh.d) +
+                       widen_bytes(&sh, M);
+  if (ws_bytes < off + need) return false;
+  q = static_cast<uint8_t*>(ws) + off;
+  s = reinterpret_cast<float*>(q + align_up((uint64_t)M * act_width(&sh)));
+  return true;
 }
 
 }  // namespace
@@ -233,10 +259,9 @@ tp_status tp_partition_weights(const tp_shape* shape, int32_t kind, const void* 
 }
 
 size_t tp_workspace_bytes(const tp_shape* shape, int32_t M, uint32_t flags) {
-  (void)flags;
   if (!shape || M < 0 || shape->t <= 0 || shape->d <= 0) return 0;
   return (size_t)(sk_bytes() + partials_bytes(shape->t, M, shape->d) + ticket_bytes(shape->d) +
-                  norm_bytes(shape->d) + widen_bytes(shape, M));
+                  norm_bytes(shape->d) + widen_bytes(shape, M) + act_bytes(shape, M, flags));
 }
 
 }  // extern "C"
@@ -251,7 +276,7 @@ using bf16 = __nv_bfloat16;
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 0;  // tcgen05 wherever the geometry allows: with PDL it wins the whole step
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
-constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK;
+constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
@@ -347,6 +372,27 @@ tp_status tc_weights(TcArgs& a, const tp_packed_desc* d, const void* w, int M, v
   return TP_OK;
 }
 
+// FP8 x FP8 (TP_F_FP8_ACT): the e4m3 weights as they are (the MMA reads them directly), the
+// activations x [M][width] quantised per token into the workspace scratch.
+tp_status x8_setup(TcArgs& a, const tp_packed_desc* d, const void* w, const bf16* x, int width, int M, void* ws,
+                   size_t ws_bytes, uint32_t flags, cudaStream_t st) {
+  uint8_t* q = nullptr;
+  float* s = nullptr;
+  if (!act_scratch(ws, ws_bytes, d->shape, M, flags, q, s) || (uint64_t)width > act_width(&d->shape))
+    return TP_ERR_WORKSPACE;
+  if (launch_quantize_fp8_per_token(x, width, M, width, q, width, s, st) != cudaSuccess) return TP_ERR_CUDA;
+  a.w = static_cast<const uint8_t*>(w);
+  a.shard_stride = d->shard_stride_bytes;
+  a.fp8 = 1;
+  a.scales_offset = d->scales_offset;
+  a.scales = reinterpret_cast<const float*>(static_cast<const uint8_t*>(w) + d->scales_offset);
+  a.scales_stride = d->shard_stride_bytes / 4;
+  a.x8 = 1;
+  a.xq = q;
+  a.tok_scales = s;
+  return TP_OK;
+}
+
 // Column-parallel half over token blocks of at most 64 (skinny) or all tokens (tcgen05).
 tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
                      int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr, size_t ws_bytes = 0) {
@@ -354,6 +400,23 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
   const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
   const size_t osz = mode == COLPAR_F32 ? 4 : 2;
+  if (d->wtype == TP_FP8_E4M3 && (flags & TP_F_FP8_ACT)) {  // e4m3 x e4m3 on the tensor cores
+    if (rows % 128 != 0 || K % 128 != 0) return TP_ERR_UNSUPPORTED;
+    TcArgs a{};
+    a.mode = mode == COLPAR_SWIGLU ? TC_COLPAR_SWIGLU : (mode == COLPAR_F32 ? TC_COLPAR_F32 : TC_COLPAR_BF16);
+    const tp_status xs = x8_setup(a, d, w, x, K, M, sk_ws, ws_bytes, flags, st);
+    if (xs != TP_OK) return xs;
+    a.t = t;
+    a.rows = rows;
+    a.K = K;
+    a.x = x;
+    a.ldx = K;
+    a.M = M;
+    a.out = out;
+    a.ldo = ldo;
+    set_streamk(a, sk_ws);
+    return launch_tc(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  }
   if (pick_tc(flags, rows, K, d->wtype == TP_FP8_E4M3, M)) {
     TcArgs a{};
     a.mode = mode == COLPAR_SWIGLU ? TC_COLPAR_SWIGLU : (mode == COLPAR_F32 ? TC_COLPAR_F32 : TC_COLPAR_BF16);
@@ -411,7 +474,9 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   const RowparPlan plan = rowpar_plan(N, t);
   if (plan.R == 0) return TP_ERR_ALIGN;
   const bool unfused = (flags & TP_F_UNFUSED_REDUCE) != 0;
-  const bool tc = pick_tc(flags, N, K, d->wtype == TP_FP8_E4M3, M);
+  const bool x8 = d->wtype == TP_FP8_E4M3 && (flags & TP_F_FP8_ACT);
+  if (x8 && (N % 128 != 0 || K % 128 != 0)) return TP_ERR_UNSUPPORTED;
+  const bool tc = x8 || pick_tc(flags, N, K, d->wtype == TP_FP8_E4M3, M);
   const bool ring = !tc && pick_ring(flags, d, N, K, M, true, ws, ws_bytes);
   const bool need_ws = !partials_user && (unfused || plan.S > 1 || tc || ring);
   float* wsP = nullptr;
@@ -428,8 +493,11 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
   if (tc) {
     TcArgs a{};
     bool pdl = (flags & TP_F_SERIAL) == 0;
-    const tp_status ws_st = tc_weights(a, d, w, M, need_ws ? ws : nullptr, ws_bytes, st, pdl);
+    const tp_status ws_st = x8 ? x8_setup(a, d, w, a_in, K * t, M, ws, ws_bytes, flags, st)
+                               : tc_weights(a, d, w, M, need_ws ? ws : nullptr, ws_bytes, st, pdl);
     if (ws_st != TP_OK) return ws_st;
+    const uint8_t* xq0 = a.xq;
+    const float* ts0 = a.tok_scales;
     a.t = t;
     a.rows = N;
     a.K = K;
@@ -456,6 +524,10 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
       a.mode = TC_ROWPAR_SHARD;
       a.x = a_in + (size_t)m0 * K * t;
+      if (x8) {
+        a.xq = xq0 + (size_t)m0 * K * t;
+        a.tok_scales = ts0 + m0;
+      }
       a.M = mb;
       a.residual = res ? res + (size_t)m0 * N : nullptr;
       a.y = y + (size_t)m0 * N;
@@ -530,7 +602,7 @@ unsigned* fused_sync(void* ws) {
 // One persistent launch for the whole block (decode token counts, bf16 or e4m3 weights), unless
 // the flags ask for separate launches or for the mma.sync kernels.
 bool pick_fused(uint32_t flags, const tp_packed_desc* d1, const tp_packed_desc* d2, int M) {
-  if (flags & (TP_F_UNFUSED_REDUCE | TP_F_KERNEL_SKINNY | TP_F_SPLIT_BLOCK)) return false;
+  if (flags & (TP_F_UNFUSED_REDUCE | TP_F_KERNEL_SKINNY | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT)) return false;
   // e4m3 decode goes to the mma.sync kernel unless the tcgen05 path is asked for
   if (d1->wtype == TP_FP8_E4M3 && !(flags & TP_F_KERNEL_TC)) return false;
   return fused_supported((int)d1->rows_per_shard, d1->shape.d, (int)d2->k_per_shard, M, d1->shape.t,
@@ -798,6 +870,15 @@ tp_status tp_attn_decode(const tp_shape* sh, const void* qkv, void* k_cache, voi
                                         static_cast<const bf16*>(qkv), static_cast<bf16*>(k_cache),
                                         static_cast<bf16*>(v_cache), lens, static_cast<bf16*>(o_in),
                                         static_cast<float*>(ws), err, S(stream)));
+}
+
+tp_status tp_quantize_fp8_per_token(const void* x, int32_t M, int32_t K, void* q, float* s, void* stream) {
+  if (M < 0 || K <= 0 || K % 8 != 0) return TP_ERR_INVALID_ARG;
+  if (M == 0) return TP_OK;
+  if (!x || !q || !s) return TP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(q) || !aligned16(s)) return TP_ERR_ALIGN;
+  return cuda_status(launch_quantize_fp8_per_token(static_cast<const bf16*>(x), K, M, K, static_cast<uint8_t*>(q), K,
+                                                   s, S(stream)));
 }
 
 size_t tp_attn_block_workspace_bytes(const tp_shape* sh, int32_t M, int32_t L, uint32_t flags) {

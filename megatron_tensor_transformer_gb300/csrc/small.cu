@@ -1,6 +1,8 @@
 // The memory-bound pieces around the two GEMM halves: the shard fold ("all-reduce"),
 // RMSNorm, and the one-token attention stand-in that maps each shard's heads.
 #include "common.cuh"
+#include <cuda_fp8.h>
+
 #include "small.h"
 
 #include <algorithm>
@@ -120,6 +122,58 @@ __global__ void widen_e4m3_kernel(const uint8_t* __restrict__ src, uint64_t src_
     o[0] = make_uint4(c0.x, c0.y, c1.x, c1.y);
     o[1] = make_uint4(c2.x, c2.y, c3.x, c3.y);
   }
+}
+
+// One CTA per token: the row's absmax (fp32 of the bf16 values), then every code.  The division
+// and the rounding are the IEEE binary32 ones the definition names (no fast reciprocal).
+__global__ void quantize_tok_kernel(const __nv_bfloat16* __restrict__ x, int ldx, int K, uint8_t* __restrict__ q,
+                                    int ldq, float* __restrict__ s) {
+  __shared__ float wmax[32];
+  const int m = blockIdx.x;
+  const __nv_bfloat16* xr = x + (size_t)m * ldx;
+  float amax = 0.f;
+  for (int k = 8 * threadIdx.x; k < K; k += 8 * blockDim.x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? wmax[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) wmax[0] = v;
+  }
+  __syncthreads();
+  const float sc = wmax[0] > 0.f ? __fdiv_rn(wmax[0], 448.0f) : 1.0f;
+  if (threadIdx.x == 0) s[m] = sc;
+  uint8_t* qr = q + (size_t)m * ldq;
+  for (int k = 8 * threadIdx.x; k < K; k += 8 * blockDim.x) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(__uint_as_float(w[i] << 16), sc), __NV_SATFINITE, __NV_E4M3);
+      const uint32_t c1 =
+          __nv_cvt_float_to_fp8(__fdiv_rn(__uint_as_float(w[i] & 0xFFFF0000u), sc), __NV_SATFINITE, __NV_E4M3);
+      o[i >> 1] |= (c0 | (c1 << 8)) << (16 * (i & 1));
+    }
+    *reinterpret_cast<uint2*>(qr + k) = make_uint2(o[0], o[1]);
+  }
+}
+
+cudaError_t launch_quantize_fp8_per_token(const __nv_bfloat16* x, int ldx, int M, int K, uint8_t* q, int ldq,
+                                          float* s, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  quantize_tok_kernel<<<M, 256, 0, st>>>(x, ldx, K, q, ldq, s);
+  note_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows, int K, int t, __nv_bfloat16* dst,

@@ -14,6 +14,11 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, fl
 // in the same per-shard layout, shards packed densely (shard s at s * rows * K elements).
 cudaError_t launch_widen_e4m3(const uint8_t* src, uint64_t src_stride, int rows, int K, int t, __nv_bfloat16* dst,
                               cudaStream_t st);
+// Per-token e4m3 quantisation of activations x [M][K] (row stride ldx): s[m] = absmax / 448 in
+// binary32 (1 for an all-zero row), q[m][k] = e4m3 RNE satfinite of x / s[m] (binary32 divide);
+// q has row stride ldq bytes.  K % 8 == 0, rows 16-byte aligned.
+cudaError_t launch_quantize_fp8_per_token(const __nv_bfloat16* x, int ldx, int M, int K, uint8_t* q, int ldq,
+                                          float* s, cudaStream_t st);
 // x[m] = row ids[m] of the vocabulary-split table (shard ids[m] / vs, row ids[m] % vs; shard s at
 // s * stride bytes, rows of d bf16), or zeros for an id outside [0, vocab).
 cudaError_t launch_embed(const uint8_t* table, uint64_t stride, int vs, int t, int vocab, int d, const int32_t* ids,

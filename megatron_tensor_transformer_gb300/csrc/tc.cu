@@ -35,8 +35,9 @@ static __device__ unsigned g_tc_error;
 constexpr int BM = 128, BK = 64;
 constexpr int kProducerWarp = 4, kMmaWarp = 5;
 
-template <int BN, bool FP8 = false>
+template <int BN, bool FP8 = false, bool X8 = false>
 struct TcCfg {
+  static constexpr int kKB = X8 ? 128 : BK;  // k per block: 128 bytes of a K-major row either way
   static constexpr int kABytes = BM * BK * 2;            // bf16 A tile the MMA reads (SW128)
   static constexpr int kAqBytes = FP8 ? BM * BK : 0;     // e4m3 A tile as TMA brings it
   static constexpr int kBBytes = BN * BK * 2;
@@ -53,11 +54,11 @@ struct Geo {  // item geometry shared by the three roles
   int n_rt, n_tt, n_items, kb_per_shard, nkb;
 };
 
-__device__ __forceinline__ Geo make_geo(const TcArgs& a, int BN) {
+__device__ __forceinline__ Geo make_geo(const TcArgs& a, int BN, int KB) {
   Geo g;
   g.n_rt = a.rows / BM;
   g.n_tt = (a.M + BN - 1) / BN;
-  g.kb_per_shard = a.K / BK;
+  g.kb_per_shard = a.K / KB;
   if (a.mode == TC_ROWPAR_CHAIN) {
     g.n_items = g.n_rt * g.n_tt;
     g.nkb = g.kb_per_shard * a.t;
@@ -141,6 +142,10 @@ __device__ __forceinline__ void raise_error(unsigned code, volatile int* abort_f
 __device__ __forceinline__ float row_scale(const TcArgs& a, int s, int p) {
   return a.scales ? a.scales[(size_t)s * a.scales_stride + p] : 1.f;
 }
+// FP8 x FP8: token m's activation scale (1 otherwise, and past the last token).
+__device__ __forceinline__ float tok_scale(const TcArgs& a, int m) {
+  return (a.tok_scales && m < a.M) ? a.tok_scales[m] : 1.f;
+}
 
 // One 16-column chunk of the accumulator for tile row p (of shard s), tokens mf..mf+15.
 template <int BN>
@@ -149,6 +154,10 @@ __device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, in
   const float sc = row_scale(a, s, p);
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = vin[j] * sc;
+  if (a.tok_scales) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] *= tok_scale(a, mf + j);
+  }
   if (a.mode == TC_COLPAR_SWIGLU) {
     // rows come as [8 gate | 8 up] blocks: the up value of row p sits 8 lanes further on
     float u[16];
@@ -313,13 +322,14 @@ __device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* sha
         const int col = e / nf, fl = e % nf, m = m0 + col;
         if (m >= a.M) continue;
         const int grow = (fl >> 3) * 16 + (fl & 7);
-        emit(a, s, rt, r0 + grow, m, sacc[col * nr + grow] * row_scale(a, s, rt * BM + r0 + grow),
-             sacc[col * nr + grow + 8] * row_scale(a, s, rt * BM + r0 + grow + 8));
+        emit(a, s, rt, r0 + grow, m, sacc[col * nr + grow] * row_scale(a, s, rt * BM + r0 + grow) * tok_scale(a, m),
+             sacc[col * nr + grow + 8] * row_scale(a, s, rt * BM + r0 + grow + 8) * tok_scale(a, m));
       }
     } else {
       for (int e = tid; e < nr * BN; e += 128) {
         const int col = e / nr, row = e % nr, m = m0 + col;
-        if (m < a.M) emit(a, s, rt, r0 + row, m, sacc[col * nr + row] * row_scale(a, s, rt * BM + r0 + row), 0.f);
+        if (m < a.M)
+          emit(a, s, rt, r0 + row, m, sacc[col * nr + row] * row_scale(a, s, rt * BM + r0 + row) * tok_scale(a, m), 0.f);
       }
     }
     if (!epi_sync(epi_bar, phase, abort_flag, 13)) return false;  // smem reused by the next item
@@ -327,10 +337,10 @@ __device__ bool streamk_fixup(const TcArgs& a, const Geo& g, const uint32_t* sha
   return true;
 }
 
-template <int BN, bool FP8>
-__global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
+template <int BN, bool FP8, bool X8 = false>
+__global__ void __launch_bounds__(TcCfg<BN, FP8, X8>::kThreadsT, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
-  using C = TcCfg<BN, FP8>;
+  using C = TcCfg<BN, FP8, X8>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
                  drain_bar = smem_u32(bars + 2 * S + 5), qfull0 = smem_u32(bars + 2 * S + 6);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const Geo g = make_geo(a, BN);
+  const Geo g = make_geo(a, BN, C::kKB);
 
   // fail fast: after a bounded wait has given up (error word set, cleared by tp_sync), later
   // launches do nothing instead of each waiting out its own timeouts
@@ -411,15 +421,15 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
           for (int kb = q.kb_lo; kb < q.kb_hi && pre < S; ++kb) {
             const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
             const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
-            pre_xcol[pre] = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
+            pre_xcol[pre] = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * C::kKB;
             pre_row[pre] = tt * BN;
             if constexpr (FP8) {  // e4m3 tile to the staging buffer, for the converter warps
               mbar_arrive_expect_tx(qfull0 + 8 * pre, C::kAqBytes);
-              tma_load_3d_hint(smem_u32(sAq + (size_t)pre * C::kAqBytes), &tmA, kk * BK, rt * BM, ss,
+              tma_load_3d_hint(smem_u32(sAq + (size_t)pre * C::kAqBytes), &tmA, kk * C::kKB, rt * BM, ss,
                                qfull0 + 8 * pre, pol_w);
             } else {
               mbar_expect_tx(full0 + 8 * pre, C::kABytes);  // stage `pre` is fresh: no empty wait
-              tma_load_3d_hint(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * pre,
+              tma_load_3d_hint(smem_u32(sA + (size_t)pre * C::kABytes), &tmA, kk * C::kKB, rt * BM, ss, full0 + 8 * pre,
                                pol_w);
             }
             ++pre;
@@ -449,15 +459,15 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
           }
           const int ss = a.mode == TC_ROWPAR_CHAIN ? kb / g.kb_per_shard : s;
           const int kk = a.mode == TC_ROWPAR_CHAIN ? kb % g.kb_per_shard : kb;
-          const int xcol = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * BK;
+          const int xcol = (a.mode >= TC_ROWPAR_SHARD ? ss * a.K : 0) + kk * C::kKB;
           if constexpr (FP8) {
             mbar_arrive_expect_tx(qfull0 + 8 * st, C::kAqBytes);
-            tma_load_3d_hint(smem_u32(sAq + (size_t)st * C::kAqBytes), &tmA, kk * BK, rt * BM, ss, qfull0 + 8 * st,
+            tma_load_3d_hint(smem_u32(sAq + (size_t)st * C::kAqBytes), &tmA, kk * C::kKB, rt * BM, ss, qfull0 + 8 * st,
                              pol_w);
             mbar_arrive_expect_tx(full0 + 8 * st, C::kBBytes);
           } else {
             mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-            tma_load_3d_hint(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * BK, rt * BM, ss, full0 + 8 * st,
+            tma_load_3d_hint(smem_u32(sA + (size_t)st * C::kABytes), &tmA, kk * C::kKB, rt * BM, ss, full0 + 8 * st,
                              pol_w);
           }
           tma_load_2d_hint(smem_u32(sB + (size_t)st * C::kBBytes), &tmB, xcol, tt * BN, full0 + 8 * st, pol_x);
@@ -467,7 +477,7 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(BM, BN);
+      constexpr uint32_t idesc = X8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN);
       int consumed = 0, it = 0;
       SegIter segs(a.streamk != 0, g);
       Seg sg;
@@ -490,8 +500,12 @@ __global__ void __launch_bounds__(TcCfg<BN, FP8>::kThreadsT, 1)
           tc_fence_after();
           const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)st * C::kBBytes);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > sg.kb_lo) || k != 0);
+          for (int k = 0; k < 4; ++k) {  // 32 bytes of each row per MMA: k16 of bf16, k32 of e4m3
+            if constexpr (X8)
+              mma_e4m3(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > sg.kb_lo) || k != 0);
+            else
+              mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > sg.kb_lo) || k != 0);
+          }
           mma_commit(empty0 + 8 * st);  // the stage is free once these MMAs have read it
           ++consumed;
         }
@@ -705,37 +719,40 @@ unsigned tc_take_device_error() {
   return v;
 }
 
-template <int BN, bool FP8>
+template <int BN, bool FP8, bool X8 = false>
 static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
-  using C = TcCfg<BN, FP8>;
+  using C = TcCfg<BN, FP8, X8>;
+  constexpr int KB = C::kKB;
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.K, (cuuint64_t)a.rows, (cuuint64_t)a.t};
-    // bf16: 128-byte-swizzled boxes the MMA reads directly; e4m3: plain 64-byte rows that the
-    // converter warps widen into that layout
-    const cuuint64_t strides[2] = {(cuuint64_t)a.K * (FP8 ? 1 : 2), (cuuint64_t)a.shard_stride};
-    const cuuint32_t box[3] = {BK, BM, 1}, es[3] = {1, 1, 1};
-    if (enc(&tmA, FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    // bf16, and e4m3 for the e4m3 x e4m3 MMA: 128-byte-swizzled boxes the MMA reads directly;
+    // e4m3 to be widened: plain 64-byte rows that the converter warps widen into that layout
+    const bool bytes = FP8 || X8;
+    const cuuint64_t strides[2] = {(cuuint64_t)a.K * (bytes ? 1 : 2), (cuuint64_t)a.shard_stride};
+    const cuuint32_t box[3] = {(cuuint32_t)KB, BM, 1}, es[3] = {1, 1, 1};
+    if (enc(&tmA, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<uint8_t*>(a.w), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             FP8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {
+  {  // activations: bf16, or (X8) their per-token e4m3 codes, [M][ldx]; boxes of 128 bytes x BN
     const cuuint64_t dims[2] = {(cuuint64_t)a.ldx, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.ldx * 2};
-    const cuuint32_t box[2] = {BK, BN}, es[2] = {1, 1};
-    if (enc(&tmB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t strides[1] = {(cuuint64_t)a.ldx * (X8 ? 1 : 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)KB, BN}, es[2] = {1, 1};
+    void* base = X8 ? static_cast<void*>(const_cast<uint8_t*>(a.xq)) : static_cast<void*>(const_cast<__nv_bfloat16*>(a.x));
+    if (enc(&tmB, X8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
   static bool attr_set = false;  // per instantiation; set before the first launch
   if (!attr_set) {
     cudaError_t e =
-        cudaFuncSetAttribute(tc_kernel<BN, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(tc_kernel<BN, FP8, X8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -744,12 +761,12 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   const int sms = sm_count() < kTcMaxGrid ? sm_count() : kTcMaxGrid;
   TcArgs b = a;
   // stream-K when the caller gave scratch for it and the tokens fit one decode tile
-  const long long nkb_item = a.mode == TC_ROWPAR_CHAIN ? (long long)a.K / BK * a.t : a.K / BK;
+  const long long nkb_item = a.mode == TC_ROWPAR_CHAIN ? (long long)a.K / KB * a.t : a.K / KB;
   // stream-K only when whole items cannot fill the GPU: its cross-CTA fix-up costs more than
   // the imbalance of item-granular scheduling once every SM has at least one item
   b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items < sms &&
               (long long)n_items * nkb_item * kTcMaxGrid < (1ll << 32);  // share table fits 32 bits
-  const long long total_kb = (long long)n_items * (a.mode == TC_ROWPAR_CHAIN ? a.K / BK * a.t : a.K / BK);
+  const long long total_kb = (long long)n_items * nkb_item;
   const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -764,21 +781,26 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   attr[1].val.cooperative = b.streamk ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, FP8>, tmA, tmB, b);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, tc_kernel<BN, FP8, X8>, tmA, tmB, b);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <bool FP8>
+template <bool FP8, bool X8 = false>
 static cudaError_t tc_bn(const TcArgs& a, cudaStream_t st, bool pdl) {
-  if (a.M <= 16) return tc_go<16, FP8>(a, st, pdl);
-  if (a.M <= 32) return tc_go<32, FP8>(a, st, pdl);
-  if (a.M <= 64) return tc_go<64, FP8>(a, st, pdl);
-  if (a.M <= 128) return tc_go<128, FP8>(a, st, pdl);
-  return tc_go<256, FP8>(a, st, pdl);
+  if (a.M <= 16) return tc_go<16, FP8, X8>(a, st, pdl);
+  if (a.M <= 32) return tc_go<32, FP8, X8>(a, st, pdl);
+  if (a.M <= 64) return tc_go<64, FP8, X8>(a, st, pdl);
+  if (a.M <= 128) return tc_go<128, FP8, X8>(a, st, pdl);
+  return tc_go<256, FP8, X8>(a, st, pdl);
 }
 
 cudaError_t launch_tc(const TcArgs& a, cudaStream_t st, bool pdl) {
+  if (a.x8) {  // e4m3 weights x e4m3 activations: k in whole 128-byte rows
+    if (a.rows % BM != 0 || a.K % 128 != 0 || a.K <= 0 || a.M <= 0 || !a.xq) return cudaErrorInvalidValue;
+    if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.xq)) & 15) return cudaErrorInvalidValue;
+    return tc_bn<false, true>(a, st, pdl);
+  }
   if (!tc_supported(a.rows, a.K, a.fp8 != 0) || a.M <= 0) return cudaErrorInvalidValue;
   if ((reinterpret_cast<uintptr_t>(a.w) | reinterpret_cast<uintptr_t>(a.x)) & 15) return cudaErrorInvalidValue;
   return a.fp8 ? tc_bn<true>(a, st, pdl) : tc_bn<false>(a, st, pdl);

@@ -40,6 +40,11 @@ struct TcArgs {
   int streamk;
   float* pieces;                  // [grid][2][BN][128] fp32
   unsigned* item_tickets;         // one per item, zero between launches
+  // FP8 x FP8 (e4m3 weights streamed as they are, activations quantised per token): xq replaces
+  // x as e4m3 codes [M, ldx] (ldx in bytes) and tok_scales [M] scales each token's outputs
+  int x8;
+  const uint8_t* xq;
+  const float* tok_scales;
 };
 
 constexpr int kTcMaxGrid = 160;          // persistent CTAs (capped so workspace sizes are fixed)

@@ -18,6 +18,7 @@ TP_BF16, TP_FP8_E4M3 = 0, 1
 TP_W_GATE_UP, TP_W_DOWN, TP_W_QKV, TP_W_O, TP_W_VOCAB, TP_W_EMBED = 0, 1, 2, 3, 4, 5
 TP_F_UNFUSED_REDUCE, TP_F_FP32_COLPAR_OUT = 0x1, 0x2
 TP_F_KERNEL_SKINNY, TP_F_KERNEL_TC, TP_F_SERIAL, TP_F_SPLIT_BLOCK = 0x10, 0x20, 0x40, 0x80
+TP_F_FP8_ACT = 0x200
 
 EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspace_bytes",
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",
@@ -25,7 +26,7 @@ EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspa
            "tp_noalloc_scratch_capacity", "tp_rmsnorm", "tp_selftest_bounded_wait",
            "tp_layer_scratch_bytes", "tp_layer_forward", "tp_selftest_e4m3_decode", "tp_sync", "tp_status_str", "tp_launch_count",
            "tp_lm_head_forward", "tp_embed_lookup", "tp_attn_workspace_bytes", "tp_attn_decode",
-           "tp_attn_block_workspace_bytes", "tp_attn_block_forward"]
+           "tp_attn_block_workspace_bytes", "tp_attn_block_forward", "tp_quantize_fp8_per_token"]
 
 
 class TpxError(RuntimeError):
@@ -85,6 +86,7 @@ def lib():
             "tp_attn_workspace_bytes": (SZ, [P(Shape), I32, I32]),
             "tp_attn_decode": (I32, [P(Shape), V, V, V, I32, V, I32, V, V, SZ, V]),
             "tp_attn_block_workspace_bytes": (SZ, [P(Shape), I32, I32, U32]),
+            "tp_quantize_fp8_per_token": (I32, [V, I32, I32, V, V, V]),
             "tp_attn_block_forward": (I32, [P(PackedDesc), V, P(PackedDesc), V, V, V, I32, V, V, I32, V, V, V, V,
                                             V, SZ, U32, V]),
             "tp_launch_count": (ctypes.c_uint64, []),
@@ -275,6 +277,13 @@ def tp_attn_block_forward(qkv, qkv_w, o, o_w, x, residual, k_cache, v_cache, len
                                        _ptr(y), _ptr(qkv_out), _ptr(o_in), _ptr(ws), ws.numel(), flags,
                                        _stream(stream)), "tp_attn_block_forward")
     return y
+
+
+def tp_quantize_fp8_per_token(x, q, s, stream=None):
+    """x: [M, K] bf16; q: [M, K] uint8 codes; s: [M] fp32 (all on the device)."""
+    _check(lib().tp_quantize_fp8_per_token(_ptr(x), x.shape[0], x.shape[1], _ptr(q), _ptr(s), _stream(stream)),
+           "tp_quantize_fp8_per_token")
+    return q, s
 
 
 def tp_attn_workspace_bytes(shape, M, L):
