@@ -665,7 +665,7 @@ tp_status tp_colpar_forward(const tp_packed_desc* desc, const void* w, const voi
   tp_status st = check_desc(desc, kind, w);
   if (st != TP_OK) return st;
   if (M < 0 || (M > 0 && (!x || !out))) return TP_ERR_INVALID_ARG;
-  if ((flags & ~(uint32_t)(TP_F_FP32_COLPAR_OUT | kKernelFlags | TP_F_SERIAL)) || bad_kernel_flags(flags))
+  if ((flags & ~(uint32_t)(TP_F_FP32_COLPAR_OUT | kKernelFlags | TP_F_SERIAL | TP_F_FP8_ACT)) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
   const bool f32 = (flags & TP_F_FP32_COLPAR_OUT) != 0;
   if (f32 && kind == TP_W_GATE_UP) return TP_ERR_INVALID_ARG;
