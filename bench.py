@@ -214,7 +214,7 @@ def run_tpx(args, rank, world, local):
     ys = {M: torch.empty((M, D), dtype=torch.bfloat16, device=dev) for M in MS}
     ws = tpx.new_workspace(sh, max(MS), dev)
     kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY,
-          "split": tpx.TP_F_SPLIT_BLOCK}[args.kernel]
+          "split": tpx.TP_F_SPLIT_BLOCK, "hilo": tpx.TP_F_FP8_HILO}[args.kernel]
     K = args.steps
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in MS] for _ in range(K)]
 
@@ -346,7 +346,7 @@ def run_layer(args, rank, world, local):
     h = torch.empty((M, ffn), dtype=torch.bfloat16, device=dev)
     K = args.steps
     kf = {"auto": 0, "tc": tpx.TP_F_KERNEL_TC, "skinny": tpx.TP_F_KERNEL_SKINNY,
-          "split": tpx.TP_F_SPLIT_BLOCK}[args.kernel] | (tpx.TP_F_FP8_ACT if x8 else 0)
+          "split": tpx.TP_F_SPLIT_BLOCK, "hilo": tpx.TP_F_FP8_HILO}[args.kernel] | (tpx.TP_F_FP8_ACT if x8 else 0)
     ws = tpx.new_workspace(sh, M, dev, flags=kf)
 
     def step():
@@ -662,7 +662,7 @@ def main():
                     sorted(LAYERS),
                     help="the headline 8B MLP decode, or a 70B-shaped layer (QKV/o_proj/MLP)")
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny", "split"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "tc", "skinny", "split", "hilo"],
                     help="force the tcgen05 or the mma.sync decode kernels, or separate launches for the "
                          "two halves of a block (default: library policy, one fused launch per block)")
     args = ap.parse_args()

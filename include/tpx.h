@@ -114,10 +114,15 @@ typedef struct {
 #define TP_F_KERNEL_SKINNY 0x10u  /* force the mma.sync weight-streaming kernel (register-direct loads) */
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernels (rows % 128, K % 64); default:
                                      tcgen05 where supported, except e4m3 weights at decode token counts
-                                     (M <= 64).  Those go to the TMA-fed mma.sync kernel (M <= 32, 128-row
-                                     tiles, k % 128, a workspace given; widening in registers, work split
-                                     evenly over two CTAs per SM, fused and unfused folds give the same
-                                     bits), else to the register-direct mma.sync kernel */
+                                     (M <= 64).  There a whole block (tp_mlp_forward, tp_proj_forward,
+                                     tp_layer_forward; 128-row tiles, k % 128) runs as one tcgen05 launch
+                                     on hi/lo activation codes (TP_F_FP8_HILO); with this flag that launch
+                                     widens the weights to bf16 instead.  The halves on their own
+                                     (tp_colpar_forward, tp_rowpar_forward, TP_F_SPLIT_BLOCK) go to the
+                                     TMA-fed mma.sync kernel (M <= 32, 128-row tiles, k % 128, a workspace
+                                     given; widening in registers, work split evenly over two CTAs per SM,
+                                     fused and unfused folds give the same bits), else to the
+                                     register-direct mma.sync kernel */
 #define TP_F_FP8_ACT 0x200u       /* e4m3 weights: also quantise each GEMM's activations per token (s_m =
                                      absmax/448 over the token's whole row, e4m3 RNE satfinite, as
                                      tp_quantize_fp8_per_token) and multiply e4m3 x e4m3 on the tensor
@@ -126,6 +131,17 @@ typedef struct {
                                      prefill: the tensor rate is twice bf16's.  tcgen05 kernels, rows %
                                      128 and k % 128; the workspace grows by M x the widest activation row
                                      (tp_workspace_bytes with this flag). */
+#define TP_F_FP8_HILO 0x400u      /* e4m3 weights, decode blocks (tp_mlp_forward, tp_proj_forward,
+                                     tp_layer_forward; M <= 64, 128-row tiles, k % 128): one persistent
+                                     tcgen05 launch per block that splits each bf16 activation exactly
+                                     into two e4m3 codes (x / s = hi + lo, s a power of two per token:
+                                     the token's row of x, or its shard's columns of h / o_in) and
+                                     multiplies e4m3 x e4m3, the weights straight from shared memory.
+                                     This is what those blocks run by default (the flag also overrides
+                                     TP_F_KERNEL_TC).  The numeric reading is unchanged (bf16 activations
+                                     times the e4m3 weights, fp32 sums, in another order); activations
+                                     below 2^-10 of the token's largest lose their lowest bits.  No
+                                     effect on bf16 weights or where the one-launch block does not apply */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, bf16 weights, 128-row
                                      and 64-k tiles) runs as ONE persistent launch: the column-parallel

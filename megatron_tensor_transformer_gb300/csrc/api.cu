@@ -276,7 +276,8 @@ using bf16 = __nv_bfloat16;
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 0;  // tcgen05 wherever the geometry allows: with PDL it wins the whole step
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
-constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT;
+constexpr uint32_t kFwdFlags =
+    TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT | TP_F_FP8_HILO;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
@@ -600,11 +601,10 @@ unsigned* fused_sync(void* ws) {
 }
 
 // One persistent launch for the whole block (decode token counts, bf16 or e4m3 weights), unless
-// the flags ask for separate launches or for the mma.sync kernels.
+// the flags ask for separate launches or for the mma.sync kernels.  e4m3 blocks split the
+// activations into hi/lo e4m3 codes, unless TP_F_KERNEL_TC alone asks for widened weights.
 bool pick_fused(uint32_t flags, const tp_packed_desc* d1, const tp_packed_desc* d2, int M) {
   if (flags & (TP_F_UNFUSED_REDUCE | TP_F_KERNEL_SKINNY | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT)) return false;
-  // e4m3 decode goes to the mma.sync kernel unless the tcgen05 path is asked for
-  if (d1->wtype == TP_FP8_E4M3 && !(flags & TP_F_KERNEL_TC)) return false;
   return fused_supported((int)d1->rows_per_shard, d1->shape.d, (int)d2->k_per_shard, M, d1->shape.t,
                          d1->wtype == TP_FP8_E4M3);
 }
@@ -619,6 +619,7 @@ tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp
   a.M = M;
   a.d = d1->shape.d;
   a.fp8 = d1->wtype == TP_FP8_E4M3;
+  a.split = a.fp8 && ((flags & TP_F_FP8_HILO) != 0 || (flags & TP_F_KERNEL_TC) == 0);
   a.w1 = static_cast<const uint8_t*>(w1);
   a.stride1 = d1->shard_stride_bytes;
   a.scales1 = d1->scales_offset;

@@ -24,6 +24,8 @@
 // scheduler), warp 5 MMA issuer.  Every wait is bounded in time; on expiry the kernel
 // records the device error word, drains, frees its TMEM and returns.
 #include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 #include "fused.h"
@@ -36,9 +38,10 @@ using namespace tc;
 namespace {
 
 constexpr int FBM = 128, FBK = 64, kRing = 8;
-constexpr int kProducer = 4, kMma = 5, kProducerB = 14;
+constexpr int kProducer = 4, kMma = 5;
 // sync words (all zero between launches)
-constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncDone = 8, kSyncTicket = 128;
+constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncXS = 4, kSyncDone = 8,
+              kSyncTicket = 128;
 
 // bf16 weights: each stage holds one 64-wide k-block, the 128 x 64 bf16 weight tile (128-byte
 // swizzle) the MMA reads from shared memory.  e4m3 weights: each stage holds a 128-wide k-block,
@@ -51,25 +54,37 @@ constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3,
 // tiles travel in a ring of their own (kSB slots, issued by a second producer warp and freed
 // by the MMA), so a weight stage is free again as soon as the converters have read it: the
 // weight ring is then almost entirely in flight from HBM.
-template <int BN, bool FP8>
+// Split activations (e4m3 weights): the weight tile goes to the MMA as it is, and four
+// converter warps split each activation tile, in place, into the e4m3 tiles hi and lo (rows 0..BN-1
+// and BN..2BN-1 of the same bytes); the MMA multiplies e4m3 x e4m3 with N = 2 BN, and the
+// epilogue adds the two column halves before the scales.
+template <int BN, bool FP8, bool SPLIT = false>
 struct FCfg {
   static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per stage
   static constexpr int kABytes = FP8 ? FBM * kKB : FBM * kKB * 2;
   static constexpr int kBSub = BN * FBK * 2;               // one 64-wide activation tile
   static constexpr int kBBytes = kBSub * (kKB / FBK);
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kSB = FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0;  // activation ring (e4m3 only)
-  static constexpr int kMaxStages = FP8 ? 10 : 8;
-  static constexpr int kRingBytes = FP8 ? 200 * 1024 - kSB * kBBytes : 200 * 1024;
+  // activation ring (e4m3 only)
+  // split: a slot is refilled only after the MMA has read it, and its tile then takes an L2 round
+  // trip and the split before the MMA can use it, so the ring must cover that whole loop
+  static constexpr int kSB = SPLIT ? (kBBytes <= 4096 ? 12 : (kBBytes <= 8192 ? 8 : 6))
+                                   : (FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0);
+  static constexpr int kMaxStages = SPLIT ? 12 : (FP8 ? 10 : 8);
+  // split: no tensor-memory A slots to feed, so more of the 227 KB goes to weights in flight
+  static constexpr int kRingBytes = (SPLIT ? 224 : 200) * 1024 - kSB * kBBytes;
   static constexpr int kUnitBytes = FP8 ? kABytes : kStageBytes;
   static constexpr int kStages = kRingBytes / kUnitBytes > kMaxStages ? kMaxStages : kRingBytes / kUnitBytes;
   static constexpr int kBSlots = FP8 ? kSB : kStages;  // activation tiles held in shared memory
   static constexpr int kASlots = 6, kACol0 = 128, kASlotCols = kKB / 2;
-  static constexpr int kTmemCols = FP8 ? 512 : (2 * BN < 32 ? 32 : 2 * BN);
-  static constexpr int kConvWarps = FP8 ? 8 : 0;
-  // converter warps from warp 6; e4m3: then the activation producer (warp 14)
+  static constexpr int kAccCols = SPLIT ? 2 * BN : BN;  // accumulator columns (hi and lo halves)
+  static constexpr int kTmemCols = SPLIT ? (4 * BN < 32 ? 32 : 4 * BN) : (FP8 ? 512 : (2 * BN < 32 ? 32 : 2 * BN));
+  static constexpr int kConvWarps = FP8 ? (SPLIT ? 4 : 8) : 0;
+  // converter warps from warp 6; e4m3: then the activation producer
+  static constexpr int kProducerB = 6 + kConvWarps;
   static constexpr int kThreads = 192 + 32 * kConvWarps + (FP8 ? 32 : 0);
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + (size_t)kBSlots * kBBytes + 1024;
+  static_assert(!SPLIT || (FP8 && BN % 8 == 0), "split activations: e4m3 weights, 8-token multiples");
 };
 
 struct FItem {
@@ -106,6 +121,9 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void raise(unsigned* err, unsigned code, volatile int* abort_flag) {
@@ -139,22 +157,87 @@ __device__ __forceinline__ float wscale(const FusedArgs& a, int stage, int s, in
   return reinterpret_cast<const float*>(b)[p];
 }
 
+// Split activations: the power of two s = 2^e with mx / s in [128, 256) (e = 0 for mx = 0).  Then
+// x / s = hi + lo exactly, hi the e4m3 rounding of x / s and lo that of the remainder: an 8-bit
+// bf16 significand fits in the two while x / s is at least 2^-2 (smaller values lose bits below
+// 2^-10 s, against a largest value of at least 2^7 s).
+__device__ __forceinline__ int split_exp(float mx) {
+  if (!(mx > 0.f) || mx > 3.0e38f) return 0;
+  const int e = (int)((__float_as_uint(mx) >> 23) & 0xFFu) - 127 - 7;
+  return e < -120 ? -120 : (e > 120 ? 120 : e);
+}
+__device__ __forceinline__ float pow2f(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
+// two bf16 (the first in the low half) times inv -> (hi, lo) e4m3 pairs
+__device__ __forceinline__ void split_pair(uint32_t xb, float inv, uint16_t& hi, uint16_t& lo) {
+  const float y0 = bf16_lo(xb) * inv, y1 = bf16_hi(xb) * inv;
+  hi = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+  const float2 hf = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+  lo = __nv_cvt_float2_to_fp8x2(make_float2(y0 - hf.x, y1 - hf.y), __NV_SATFINITE, __NV_E4M3);
+}
+// the per-(shard, token) maxima of |stage-2 input| and the per-token maxima of |x| (float bits)
+__device__ __forceinline__ unsigned* hmax_of(const FusedArgs& a) { return a.sync + fused_hmax_off(a.d); }
+__device__ __forceinline__ unsigned* xmax_of(const FusedArgs& a) {
+  return a.sync + fused_hmax_off(a.d) + 8 * kFusedMaxMWords;
+}
+// the split scale 2^e of a token from its maximum's bits
+__device__ __forceinline__ int split_exp_bits(const unsigned* p) { return split_exp(__uint_as_float(__ldcg(p))); }
+__device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// Bounded wait (~2 s) until every CTA has added its share of the maxima of |x|.
+__device__ bool wait_xmax(const FusedArgs& a, volatile int* abort_flag) {
+  const unsigned* cnt = a.sync + kSyncXS;
+  if (ld_acquire(cnt) < gridDim.x) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; ld_acquire(cnt) < gridDim.x; ++i) {
+      if (*abort_flag) return false;
+      if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
+        raise(a.err, 44, abort_flag);
+        return false;
+      }
+      __nanosleep(64);
+    }
+  }
+  return true;
+}
+// The largest |value| a warp's lanes hold for each of 16 tokens, into the shard's maxima
+// (non-negative floats order like their bits).
+__device__ __forceinline__ void warp_token_max(const FusedArgs& a, int s, int mf, float (&mv)[16]) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mv[j] = fmaxf(mv[j], __shfl_xor_sync(0xffffffffu, mv[j], o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (mf + j < a.M && mv[j] > 0.f) atomicMax(hmax_of(a) + s * kFusedMaxMWords + mf + j, __float_as_uint(mv[j]));
+  }
+}
+
 // Stage-1 epilogue for one 16-token chunk of tile row p (packed row of shard s).
-template <int KIND>
+template <int KIND, bool SPLIT>
 __device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, int mf, const float (&v)[16]) {
   if (KIND == FUSED_MLP) {
     // rows come as [8 gate | 8 up] blocks: the up value of row p sits 8 lanes further on
     float u[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) u[j] = __shfl_down_sync(0xffffffffu, v[j], 8);
+    float mv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) mv[j] = 0.f;
     if ((p & 15) < 8) {
       const int ldh = a.t * (a.rows1 / 2);
       const int f = s * (a.rows1 / 2) + (p >> 4) * 8 + (p & 7);
       uint16_t* h = reinterpret_cast<uint16_t*>(a.mid);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        if (mf + j < a.M) h[(size_t)(mf + j) * ldh + f] = f2bf(silu_f(v[j]) * u[j]);
+        if (mf + j < a.M) {
+          const uint16_t hb = f2bf(silu_f(v[j]) * u[j]);
+          h[(size_t)(mf + j) * ldh + f] = hb;
+          mv[j] = fabsf(__uint_as_float((uint32_t)hb << 16));
+        }
     }
+    if constexpr (SPLIT) warp_token_max(a, s, mf, mv);
   } else {
     // qkv column s*rows1 + p; a v row also becomes o_in for every q head of its group
     const int ldq = a.t * a.rows1, nqs = a.n_q / a.t, nkvs = a.n_kv / a.t, G = a.n_q / a.n_kv;
@@ -164,14 +247,21 @@ __device__ __forceinline__ void stage1_chunk(const FusedArgs& a, int s, int p, i
     const int ldo = a.n_q * a.hd;
     const bool vrow = p >= vb;
     const int j = vrow ? (p - vb) / a.hd : 0, e = vrow ? (p - vb) % a.hd : 0;
+    float mv[16];
 #pragma unroll
     for (int jj = 0; jj < 16; ++jj) {
+      mv[jj] = 0.f;
       const int m = mf + jj;
-      if (m >= a.M) break;
+      if (m >= a.M) continue;
       const uint16_t b = f2bf(v[jj]);
       q[(size_t)m * ldq + (size_t)s * a.rows1 + p] = b;
-      if (vrow)
+      if (vrow) {
         for (int g = 0; g < G; ++g) o[(size_t)m * ldo + (size_t)(s * nqs + j * G + g) * a.hd + e] = b;
+        mv[jj] = fabsf(__uint_as_float((uint32_t)b << 16));
+      }
+    }
+    if constexpr (SPLIT) {
+      if (__any_sync(0xffffffffu, vrow)) warp_token_max(a, s, mf, mv);  // only v rows feed o_in
     }
   }
 }
@@ -253,11 +343,13 @@ __device__ __forceinline__ void input_norm(const FusedArgs& a) {
   }
 }
 
-template <int BN, int KIND, bool FP8>
-__global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
+template <int BN, int KIND, bool FP8, bool SPLIT>
+__global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
                  const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2, FusedArgs a) {
-  using C = FCfg<BN, FP8>;
+  using C = FCfg<BN, FP8, SPLIT>;
+  constexpr int kProducerB = C::kProducerB;
+  constexpr int kSplitBars = SPLIT ? C::kSB : 0;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -265,8 +357,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
   uint8_t* sB = smem + (size_t)S * C::kABytes;   // kBSlots x [BN rows x kKB] bf16, SW128 tiles of 64
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)C::kBSlots * C::kBBytes);
   // bars: full[S], empty[S], tfull[2], tempty[2], ifull[kRing], iempty[kRing], drain, afull[kASlots],
-  // aempty[kASlots], fullB[kSB], emptyB[kSB]
-  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1 + 2 * C::kASlots + 2 * C::kSB);
+  // aempty[kASlots], fullB[kSB], emptyB[kSB], (split activations) splitB[kSB]
+  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1 + 2 * C::kASlots + 2 * C::kSB + kSplitBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 2);
@@ -277,7 +369,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
                  tempty0 = smem_u32(bars + 2 * S + 2), ifull0 = smem_u32(bars + 2 * S + 4),
                  iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing),
                  afull0 = drain_bar + 8, aempty0 = drain_bar + 8 + 8 * C::kASlots,
-                 fullB0 = aempty0 + 8 * C::kASlots, emptyB0 = fullB0 + 8 * C::kSB;
+                 fullB0 = aempty0 + 8 * C::kASlots, emptyB0 = fullB0 + 8 * C::kSB, splitB0 = emptyB0 + 8 * C::kSB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n1 = a.t * (a.rows1 / FBM), ntot = n1 + a.t * (a.d / FBM);
 
@@ -290,7 +382,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(full0 + 8 * i, 1);
-      mbar_init(empty0 + 8 * i, FP8 ? C::kConvWarps : 1);  // e4m3: freed by the converters
+      // e4m3 widened: freed by the converters; otherwise by the MMA's commit
+      mbar_init(empty0 + 8 * i, FP8 && !SPLIT ? C::kConvWarps : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
@@ -311,6 +404,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
         mbar_init(fullB0 + 8 * i, 1);
         mbar_init(emptyB0 + 8 * i, 1);  // tcgen05.commit after the MMAs that read the tile
       }
+      for (int i = 0; i < kSplitBars; ++i) mbar_init(splitB0 + 8 * i, C::kConvWarps);  // split in place
     }
     *abort_flag = 0;
     *mma_consumed = 0;
@@ -470,7 +564,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
     }
   } else if (warp == kMma) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(FBM, BN);
+      constexpr uint32_t idesc = SPLIT ? idesc_e4m3(FBM, 2 * BN) : idesc_bf16(FBM, BN);
       int q = 0, it = 0, consumed = 0;
       while (!*abort_flag) {
         const int r = q % kRing;
@@ -489,43 +583,64 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
         bool ok = true;
-        for (int kb = 0; kb < f.nkb; ++kb) {
-          // the activation tile: in the weight stage (bf16), or in its own ring (e4m3)
-          constexpr int NB = FP8 ? C::kSB : S;
-          const int st = consumed % NB;
-          if (!mbar_wait((FP8 ? fullB0 : full0) + 8 * st, (consumed / NB) & 1)) {
-            raise(a.err, 28, abort_flag);
-            ok = false;
-            break;
-          }
-          const uint32_t bb = smem_u32(sB + (size_t)st * C::kBBytes);
-          if constexpr (FP8) {
-            // the widened weight tile of this k-block waits in tensor-memory slot `slot`
-            const int slot = consumed % C::kASlots;
-            if (!mbar_wait(afull0 + 8 * slot, (consumed / C::kASlots) & 1)) {
-              raise(a.err, 33, abort_flag);
+        if constexpr (SPLIT) {
+          for (int kb = 0; kb < f.nkb; ++kb) {
+            // the weight stage as it landed, and the activation tile once split into hi | lo
+            const int st = consumed % S, sl = consumed % C::kSB;
+            if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1) ||
+                !mbar_wait(splitB0 + 8 * sl, (consumed / C::kSB) & 1)) {
+              raise(a.err, 45, abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t at = tmem_base + (uint32_t)(C::kACol0 + C::kASlotCols * slot);
+            const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)sl * C::kBBytes);
 #pragma unroll
-            for (int k = 0; k < C::kKB / 16; ++k)
-              mma_bf16_tmem_a(d, at + 8 * k, sw128_desc(bb + (k / 4) * C::kBSub + 32 * (k % 4)), idesc,
-                              (kb > 0) || k != 0);
-            mma_commit(emptyB0 + 8 * st);
-            mma_commit(aempty0 + 8 * slot);
-          } else {
-            tc_fence_after();
-            const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes);
-#pragma unroll
-            for (int k = 0; k < FBK / 16; ++k)
-              mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+            for (int k = 0; k < C::kKB / 32; ++k)
+              mma_e4m3(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
             mma_commit(empty0 + 8 * st);
+            mma_commit(emptyB0 + 8 * sl);
+            ++consumed;
           }
-          ++consumed;
+        } else {
+          for (int kb = 0; kb < f.nkb; ++kb) {
+            // the activation tile: in the weight stage (bf16), or in its own ring (e4m3)
+            constexpr int NB = FP8 ? C::kSB : S;
+            const int st = consumed % NB;
+            if (!mbar_wait((FP8 ? fullB0 : full0) + 8 * st, (consumed / NB) & 1)) {
+              raise(a.err, 28, abort_flag);
+              ok = false;
+              break;
+            }
+            const uint32_t bb = smem_u32(sB + (size_t)st * C::kBBytes);
+            if constexpr (FP8) {
+              // the widened weight tile of this k-block waits in tensor-memory slot `slot`
+              const int slot = consumed % C::kASlots;
+              if (!mbar_wait(afull0 + 8 * slot, (consumed / C::kASlots) & 1)) {
+                raise(a.err, 33, abort_flag);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t at = tmem_base + (uint32_t)(C::kACol0 + C::kASlotCols * slot);
+#pragma unroll
+              for (int k = 0; k < C::kKB / 16; ++k)
+                mma_bf16_tmem_a(d, at + 8 * k, sw128_desc(bb + (k / 4) * C::kBSub + 32 * (k % 4)), idesc,
+                                (kb > 0) || k != 0);
+              mma_commit(emptyB0 + 8 * st);
+              mma_commit(aempty0 + 8 * slot);
+            } else {
+              tc_fence_after();
+              const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes);
+#pragma unroll
+              for (int k = 0; k < FBK / 16; ++k)
+                mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+              mma_commit(empty0 + 8 * st);
+            }
+            ++consumed;
+          }
         }
         if (!ok) break;
         mma_commit(tfull0 + 8 * acc);
@@ -578,7 +693,118 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       }
     }
   } else if (warp >= 6) {
-    if constexpr (FP8) {
+    if constexpr (SPLIT) {
+      // Split converters.  First the per-token maxima of |x|: each CTA reduces a slice of the
+      // columns of every token, adds it (atomic max) to the grid's maxima and counts itself in.
+      __shared__ unsigned s_xmax[kFusedMaxM];
+      const int cw = warp - 6, ct = 32 * cw + lane;
+      griddep_wait();
+      if (ct < kFusedMaxM) s_xmax[ct] = 0u;
+      conv_bar();
+      {
+        const int nch = a.d / 8;  // 16-byte chunks of a row
+        const int c_lo = (int)((long long)nch * blockIdx.x / gridDim.x);
+        const int cnt = (int)((long long)nch * (blockIdx.x + 1) / gridDim.x) - c_lo;
+        for (int i = ct; i < a.M * cnt; i += 32 * C::kConvWarps) {
+          const int m = i / cnt, c = c_lo + i % cnt;
+          const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.d + 8 * c);
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+          float mx = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
+          if (mx > 0.f) atomicMax(s_xmax + m, __float_as_uint(mx));
+        }
+      }
+      conv_bar();
+      if (ct < a.M && s_xmax[ct] != 0u) atomicMax(xmax_of(a) + ct, s_xmax[ct]);
+      conv_bar();  // then one release by thread 0 covers the group's atomics (barrier, then release)
+      if (ct == 0) red_release_add(a.sync + kSyncXS, 1u);
+      bool ok = wait_xmax(a, abort_flag);
+      // each warp splits BN/4 tokens, 8 lanes a token, lane l the 16-wide k chunk l % 8
+      constexpr int NIT = BN / 16;
+      const int c = lane & 7;
+      int tok[NIT];
+      float inv1[NIT];
+#pragma unroll
+      for (int it = 0; it < NIT; ++it) {
+        tok[it] = cw * (BN / 4) + 4 * it + (lane >> 3);
+        inv1[it] = tok[it] < a.M ? pow2f(-split_exp_bits(xmax_of(a) + tok[it])) : 1.f;
+      }
+      // per shard, the split exponents of this warp's tokens, once the shard's stage 1 is known done
+      __shared__ signed char s_exp[8][kFusedMaxM];
+      unsigned shard_seen = 0u;
+      int q = 0, kq = 0;
+      while (ok) {
+        const int rr = q % kRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(ifull0 + 8 * rr, (q / kRing) & 1))) {
+          raise(a.err, 46, abort_flag);
+          break;
+        }
+        const int id = ring[rr];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(iempty0 + 8 * rr);
+        ++q;
+        if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
+        const FItem f = fdecode(a, id, C::kKB);
+        float inv[NIT];
+        if (f.stage == 1) {
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) inv[it] = inv1[it];
+        } else {
+          if (!(shard_seen >> f.s & 1u)) {
+            // the shard's stage-1 items are done, so the maxima of its h (or o_in) are final
+            if (!__all_sync(0xffffffffu, wait_stage1(a, f.s, abort_flag))) break;
+#pragma unroll
+            for (int it = 0; it < NIT; ++it)
+              if (c == 0)
+                s_exp[f.s][tok[it]] =
+                    (signed char)(tok[it] < a.M ? split_exp_bits(hmax_of(a) + f.s * kFusedMaxMWords + tok[it]) : 0);
+            shard_seen |= 1u << f.s;
+            __syncwarp();
+          }
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) inv[it] = pow2f(-(int)s_exp[f.s][tok[it]]);
+        }
+        for (int kb = 0; kb < f.nkb; ++kb, ++kq) {
+          const int sl = kq % C::kSB;
+          if (!__all_sync(0xffffffffu, mbar_wait(fullB0 + 8 * sl, (kq / C::kSB) & 1))) {
+            raise(a.err, 47, abort_flag);
+            ok = false;
+            break;
+          }
+          // token m's bf16 rows (k 0..63 in the first 64-wide box, 64..127 in the second) are
+          // the bytes of its e4m3 rows hi = m and lo = BN + m: read all of them, then write
+          uint8_t* tile = sB + (size_t)sl * C::kBBytes;
+          uint4 v0[NIT], v1[NIT];
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) {
+            const int m = tok[it], sw = m & 7, cc = 2 * (c & 3);
+            const uint8_t* row = tile + (c >> 2) * C::kBSub + 128 * m;
+            v0[it] = *reinterpret_cast<const uint4*>(row + 16 * (cc ^ sw));
+            v1[it] = *reinterpret_cast<const uint4*>(row + 16 * ((cc + 1) ^ sw));
+          }
+          __syncwarp();
+#pragma unroll
+          for (int it = 0; it < NIT; ++it) {
+            const uint32_t w[8] = {v0[it].x, v0[it].y, v0[it].z, v0[it].w, v1[it].x, v1[it].y, v1[it].z, v1[it].w};
+            uint16_t hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) split_pair(w[j], inv[it], hi[j], lo[j]);
+            uint4 H, L;
+            H.x = hi[0] | ((uint32_t)hi[1] << 16); H.y = hi[2] | ((uint32_t)hi[3] << 16);
+            H.z = hi[4] | ((uint32_t)hi[5] << 16); H.w = hi[6] | ((uint32_t)hi[7] << 16);
+            L.x = lo[0] | ((uint32_t)lo[1] << 16); L.y = lo[2] | ((uint32_t)lo[3] << 16);
+            L.z = lo[4] | ((uint32_t)lo[5] << 16); L.w = lo[6] | ((uint32_t)lo[7] << 16);
+            const int m = tok[it], off = 16 * (c ^ (m & 7));
+            *reinterpret_cast<uint4*>(tile + 128 * m + off) = H;
+            *reinterpret_cast<uint4*>(tile + 128 * (BN + m) + off) = L;
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(splitB0 + 8 * sl);
+        }
+      }
+    } else if constexpr (FP8) {
       // converter warps: warp w may address TMEM lanes 32(w%4)..+31, so it widens those rows;
       // of the two warps of a quarter, warp `sub` takes the 64-wide half `sub` of the stage's
       // 128-wide k-block.  Each thread takes one row: 64 e4m3 codes (four 16-byte chunks, which
@@ -654,7 +880,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       epi_bar();
       if (threadIdx.x == 0) red_release_add(a.sync + kSyncInNorm, 1u);
     }
-    bool scale_ready = a.in_norm == 0;
+    bool scale_ready = a.in_norm == 0, xmax_ready = false;
     int q = 0, it = 0;
     while (true) {
       const int rr = q % kRing;
@@ -669,14 +895,32 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
       const FItem f = fdecode(a, id, C::kKB);
       const int acc = it & 1;
+      // fetched while the item's MMAs run: the row's fp32 scale (e4m3), and (split activations)
+      // the first 16 tokens' scales 2^e
+      const int p = f.rt * FBM + r;
+      const float wsc = FP8 ? wscale(a, f.stage, f.s, p) : 1.f;
+      const unsigned* split_max = nullptr;  // the maxima the item's activations were split by
+      float tsc0[16];
+      if constexpr (SPLIT) {
+        if (f.stage == 1) {
+          if (!xmax_ready) {
+            if (!__all_sync(0xffffffffu, wait_xmax(a, abort_flag))) break;
+            xmax_ready = true;
+          }
+          split_max = xmax_of(a);
+        } else {
+          if (!__all_sync(0xffffffffu, wait_stage1(a, f.s, abort_flag))) break;
+          split_max = hmax_of(a) + f.s * kFusedMaxMWords;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tsc0[j] = j < a.M ? pow2f(split_exp_bits(split_max + j)) : 0.f;
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
         raise(a.err, 31, abort_flag);
         break;
       }
       tc_fence_after();
-      const uint32_t tb = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(warp * 32) << 16);
-      const int p = f.rt * FBM + r;
-      const float wsc = FP8 ? wscale(a, f.stage, f.s, p) : 1.f;  // e4m3: the row's fp32 scale
+      const uint32_t tb = tmem_base + (uint32_t)(acc * C::kAccCols) + ((uint32_t)(warp * 32) << 16);
       const bool tok_scale = f.stage == 1 && a.in_scale != nullptr;
       if (tok_scale && !scale_ready) {  // wait (bounded) for CTA 0's input norm
         const uint64_t t0 = globaltimer_ns();
@@ -693,8 +937,19 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       for (int c0 = 0; c0 < BN; c0 += 16) {
         float v[16];
         tmem_ld16(tb + c0, v);
-        tmem_ld_wait();
-        if constexpr (FP8) {
+        if constexpr (SPLIT) {
+          float w[16];
+          tmem_ld16(tb + BN + c0, w);  // the lo half
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float ts = c0 == 0 ? tsc0[j] : (c0 + j < a.M ? pow2f(split_exp_bits(split_max + c0 + j)) : 0.f);
+            v[j] = ((v[j] + w[j]) * wsc) * ts;
+          }
+        } else {
+          tmem_ld_wait();
+        }
+        if constexpr (FP8 && !SPLIT) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] *= wsc;
         }
@@ -703,7 +958,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
           for (int j = 0; j < 16; ++j) v[j] *= __ldcg(a.in_scale + c0 + j);
         }
         if (f.stage == 1) {
-          stage1_chunk<KIND>(a, f.s, p, c0, v);
+          stage1_chunk<KIND, SPLIT>(a, f.s, p, c0, v);
         } else {
           float* P = a.partials + (size_t)f.s * a.M * a.d + p;
 #pragma unroll
@@ -760,18 +1015,20 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
   __syncthreads();
   // drain: wait (bounded) for any TMA copy issued but never consumed
   if (warp == kProducer && lane == 0) {
-    for (int qq = FP8 ? *conv_consumed : *mma_consumed; qq < issued; ++qq)
+    for (int qq = FP8 && !SPLIT ? *conv_consumed : *mma_consumed; qq < issued; ++qq)
       if (!mbar_wait(full0 + 8 * (qq % S), (qq / S) & 1)) {
         atomicExch(a.err, 32u);
         break;
       }
   }
-  if (FP8 && warp == kProducerB && lane == 0) {
-    for (int qq = *mma_consumed; qq < issuedB; ++qq)
-      if (!mbar_wait(fullB0 + 8 * (qq % C::kSB), (qq / C::kSB) & 1)) {
-        atomicExch(a.err, 38u);
-        break;
-      }
+  if constexpr (FP8) {
+    if (warp == kProducerB && lane == 0) {
+      for (int qq = *mma_consumed; qq < issuedB; ++qq)
+        if (!mbar_wait(fullB0 + 8 * (qq % C::kSB), (qq / C::kSB) & 1)) {
+          atomicExch(a.err, 38u);
+          break;
+        }
+    }
   }
   __syncthreads();
   if (warp == kMma) {
@@ -785,6 +1042,10 @@ __global__ void __launch_bounds__(FCfg<BN, FP8>::kThreads, 1)
       a.sync[kSyncItem] = 0u;
       a.sync[kSyncInNorm] = 0u;
       for (int s = 0; s < 8; ++s) a.sync[kSyncDone + s] = 0u;
+      if (SPLIT) {
+        a.sync[kSyncXS] = 0u;
+        for (int i = 0; i < 9 * kFusedMaxMWords; ++i) hmax_of(a)[i] = 0u;  // h maxima, then x maxima
+      }
       if (*reinterpret_cast<volatile unsigned*>(a.err) != 0u) {
         for (int rt = 0; rt < a.d / FBM; ++rt) a.sync[kSyncTicket + rt] = 0u;
         a.sync[kSyncNormTiles] = 0u;
@@ -803,9 +1064,9 @@ bool fused_supported(int rows1, int d, int K2, int M, int t, bool fp8) {
          d > 0 && d % kkb == 0 && K2 % kkb == 0 && K2 > 0 && fused_sync_words(d) <= kTcMaxStreamkItems - 64;
 }
 
-template <int BN, int KIND, bool FP8>
+template <int BN, int KIND, bool FP8, bool SPLIT>
 static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
-  using C = FCfg<BN, FP8>;
+  using C = FCfg<BN, FP8, SPLIT>;
   // weights: 128-byte box rows in the 128-byte swizzle: bf16 boxes of 64 columns the MMA reads,
   // or e4m3 boxes of 128 columns the converter warps read
   const CUtensorMapDataType wty = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -854,7 +1115,8 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   static bool attr_set = false;  // per instantiation
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(fused_kernel<BN, KIND, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        cudaFuncSetAttribute(fused_kernel<BN, KIND, FP8, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -878,16 +1140,16 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND, FP8>, tm[0], tm[1], tm[2], tm[3], a);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_kernel<BN, KIND, FP8, SPLIT>, tm[0], tm[1], tm[2], tm[3], a);
   note_launch();
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int KIND, bool FP8>
+template <int KIND, bool FP8, bool SPLIT = false>
 static cudaError_t fused_bn(const FusedArgs& a, cudaStream_t st, bool pdl) {
-  if (a.M <= 16) return fused_go<16, KIND, FP8>(a, st, pdl);
-  if (a.M <= 32) return fused_go<32, KIND, FP8>(a, st, pdl);
-  return fused_go<64, KIND, FP8>(a, st, pdl);
+  if (a.M <= 16) return fused_go<16, KIND, FP8, SPLIT>(a, st, pdl);
+  if (a.M <= 32) return fused_go<32, KIND, FP8, SPLIT>(a, st, pdl);
+  return fused_go<64, KIND, FP8, SPLIT>(a, st, pdl);
 }
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
@@ -896,6 +1158,10 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   if ((reinterpret_cast<uintptr_t>(a.w1) | reinterpret_cast<uintptr_t>(a.w2) | reinterpret_cast<uintptr_t>(a.x) |
        reinterpret_cast<uintptr_t>(a.mid2)) & 15)
     return cudaErrorInvalidValue;
+  if (a.split && !a.fp8) return cudaErrorInvalidValue;
+  if (a.split)
+    return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP, true, true>(a, st, pdl)
+                               : fused_bn<FUSED_PROJ, true, true>(a, st, pdl);
   if (a.fp8) return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP, true>(a, st, pdl) : fused_bn<FUSED_PROJ, true>(a, st, pdl);
   return a.kind == FUSED_MLP ? fused_bn<FUSED_MLP, false>(a, st, pdl) : fused_bn<FUSED_PROJ, false>(a, st, pdl);
 }

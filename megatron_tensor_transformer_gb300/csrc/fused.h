@@ -44,14 +44,21 @@ struct FusedArgs {
   float* out_rms;
   float* norm_ss;
   float eps;
+  // e4m3 weights, split activations: instead of widening the weights, each activation tile is
+  // split exactly into two e4m3 tiles (x / s = hi + lo, s a power of two per token: over the
+  // whole row for x, over the shard's columns for h or o_in) and the MMA multiplies e4m3 x e4m3
+  int split;
 };
 
 constexpr int kFusedMaxM = 64;
 constexpr int kFusedMaxMWords = 64;  // per-token arrays are sized for kFusedMaxM tokens
 // fp32 words of RMSNorm scratch a fused block with a folded norm needs: norm_ss, in_scale, out_rms
 inline int fused_norm_words(int d) { return kFusedMaxMWords * (d / 128) + 2 * kFusedMaxMWords; }
-// words of the sync area the fused kernel uses: 128 + one ticket per 128-row output tile
-inline int fused_sync_words(int d) { return 128 + d / 128; }
+// Sync area words: 128 + one ticket per 128-row output tile, then (split activations) the
+// per-(shard, token) maxima of the stage-2 input [8][64] (zero between launches) and the
+// input's per-token scales [64].
+__host__ __device__ inline int fused_hmax_off(int d) { return (128 + d / 128 + 31) / 32 * 32; }
+inline int fused_sync_words(int d) { return fused_hmax_off(d) + 8 * kFusedMaxMWords + kFusedMaxMWords; }
 
 // Whether the fused kernel supports this block (128-row tiles, M <= 64; 64-wide k-blocks for bf16
 // weights, 128-wide for e4m3).

@@ -200,12 +200,13 @@ def _fp8_proj(d, n_q, n_kv, hd, t, M, dev, seed, flags=0):
     return qkv, qkv_ref[:, cols], y, y_ref
 
 
-@pytest.mark.parametrize("flags", [TC, 0], ids=["tcgen05-fused", "default"])
+@pytest.mark.parametrize("flags", [TC, 0, SPLIT], ids=["widened", "default-hilo", "halves"])
 @pytest.mark.parametrize("t,M", [(1, 16), (2, 5), (4, 64), (8, 16)])
 def test_fused_fp8_blocks_vs_oracle(dev, t, M, flags):
     """Against the oracle on the dequantised weights; the bf16 bar (stricter than the 3e-2 FP8
-    bar) holds for both blocks, on the fused tcgen05 path and on the default e4m3 decode path
-    (the mma.sync kernel)."""
+    bar) holds for both blocks: the one-launch block widening the weights (TP_F_KERNEL_TC), the
+    default one-launch block on hi/lo activation codes, and the halves in separate launches
+    (the mma.sync kernels)."""
     m = Mlp(2048, 7168, t, M, dev, seed=13, wtype=FP8)
     y, h = m.run(flags=flags)
     y_ref, h_ref = m.oracle()

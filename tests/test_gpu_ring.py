@@ -1,5 +1,6 @@
-"""The TMA-fed e4m3 decode kernel (1..32 tokens) through the C ABI, against the float64 oracle
-on the dequantised weights: the MLP block (gate/up + SwiGLU, down + the shard fold) and the
+"""The TMA-fed e4m3 decode kernel (1..32 tokens) through the C ABI, reached as the blocks' halves
+in separate launches (TP_F_SPLIT_BLOCK; a whole decode block is one hi/lo launch by default),
+against the float64 oracle on the dequantised weights: the MLP block (gate/up + SwiGLU, down + the shard fold) and the
 attention projections (QKV, o_proj), for t in {1, 2, 4, 8} and ragged token counts; shapes
 small enough that every (shard, row tile) is split across CTAs, so the pieces are merged;
 the fused fold bit-equal to the unfused partials + fold path; repeat runs bit-identical."""
@@ -12,6 +13,7 @@ from oracle import tp_oracle as O
 from tests.test_gpu_parity import REL_F, REL_F_FP8, Mlp, bits, check_close
 
 pytestmark = pytest.mark.gpu
+SB = tpx.TP_F_SPLIT_BLOCK  # the halves as separate launches: the ring kernel for e4m3 decode
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -25,7 +27,7 @@ def dev():
     return torch.device("cuda:0")
 
 
-def check_mlp(m, flags=0, residual=True):
+def check_mlp(m, flags=SB, residual=True):
     y, h = m.run(residual=residual, flags=flags)
     assert tpx.tp_sync(timeout_ms=20000) == tpx.TP_OK
     y_ref, h_ref = m.oracle(residual=residual)
@@ -52,18 +54,18 @@ def test_ring_every_tile_split_into_pieces(dev):
 
 def test_ring_fused_fold_bits_equal_unfused(dev):
     m = Mlp(1024, 4096, 8, 16, dev, seed=5, wtype=tpx.TP_FP8_E4M3)
-    y0, h0 = m.run()
-    y1, h1 = m.run(flags=tpx.TP_F_UNFUSED_REDUCE)
+    y0, h0 = m.run(flags=SB)
+    y1, h1 = m.run(flags=SB | tpx.TP_F_UNFUSED_REDUCE)
     assert torch.equal(h0.view(torch.int16), h1.view(torch.int16))
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
-    y2, _ = m.run()
+    y2, _ = m.run(flags=SB)
     assert torch.equal(y0.view(torch.int16), y2.view(torch.int16))
 
 
 def test_ring_agrees_with_the_mma_sync_kernel(dev):
     """Both e4m3 decode kernels against each other (different k orders: close, not equal)."""
     m = Mlp(2048, 7168, 8, 16, dev, seed=6, wtype=tpx.TP_FP8_E4M3)
-    y0, _ = m.run()
+    y0, _ = m.run(flags=SB)
     y1, _ = m.run(flags=tpx.TP_F_KERNEL_SKINNY)
     assert O.rel_frobenius(bits(y0), O.as_f64(bits(y1))) <= 2e-3
 
@@ -80,7 +82,7 @@ def test_ring_attention_projections(dev, t, M):
     qkv = torch.full((M, Q), float("nan"), dtype=torch.bfloat16, device=dev)
     o_in = torch.full((M, n_q * hd), float("nan"), dtype=torch.bfloat16, device=dev)
     ws = tpx.new_workspace(sh, M, dev)
-    tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y, qkv, o_in, ws)
+    tpx.tp_proj_forward(q, q_w, o, o_w, x, x, y, qkv, o_in, ws, SB)
     assert tpx.tp_sync(timeout_ms=20000) == tpx.TP_OK
     deq = []
     for w in (wqkv, wo):

@@ -125,8 +125,12 @@ def test_405b_layer_full_size_sampled_tokens(dev):
     check_layer(bits(y), lay.oracle(bits(x)), what="405B layer, 2 tokens")
 
 
-@pytest.mark.parametrize("M,wtype", [(16, tpx.TP_BF16), (5, tpx.TP_BF16), (16, tpx.TP_FP8_E4M3)])
-def test_layer_norm_folded_into_blocks(dev, M, wtype):
+@pytest.mark.parametrize("M,wtype,fl", [(16, tpx.TP_BF16, 0), (5, tpx.TP_BF16, 0),
+                                        (16, tpx.TP_FP8_E4M3, tpx.TP_F_KERNEL_TC),
+                                        (16, tpx.TP_FP8_E4M3, tpx.TP_F_FP8_HILO),
+                                        (40, tpx.TP_FP8_E4M3, tpx.TP_F_FP8_HILO)],
+                         ids=["bf16-16", "bf16-5", "fp8-widened-16", "fp8-split-16", "fp8-split-40"])
+def test_layer_norm_folded_into_blocks(dev, M, wtype, fl):
     """Decode layers run as two launches: the RMSNorms become per-token factors on the
     column-parallel accumulators (the attention block computes its input's factors, and its
     fold those of h1).  Against the oracle, against the path with separate RMSNorm launches
@@ -145,7 +149,7 @@ def test_layer_norm_folded_into_blocks(dev, M, wtype):
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, d), 1.0, 4, inputs.STREAM_X, dev)
-    fl = 0 if wtype == tpx.TP_BF16 else tpx.TP_F_KERNEL_TC  # e4m3 decode is fused only when asked
+    # e4m3 decode is fused only when asked (widened weights, or split activations)
     n0 = tpx.tp_launch_count()
     y = lay.gpu(x, scratch, ws, fl)
     assert tpx.tp_launch_count() - n0 == 2
