@@ -143,11 +143,13 @@ typedef struct {
                                      below 2^-10 of the token's largest lose their lowest bits.  No
                                      effect on bf16 weights or where the one-launch block does not apply */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
-                                     launches.  By default a decode block (M <= 64, bf16 weights, 128-row
-                                     and 64-k tiles) runs as ONE persistent launch: the column-parallel
-                                     items, then the row-parallel items, each of which waits only for its
-                                     own shard's first half; the last shard of each 128-row output tile
-                                     folds the t partials in shard order (same bits as the split path) */
+                                     launches.  By default a decode block (M <= 64, 128-row tiles; k %
+                                     64 for bf16 weights, k % 128 for e4m3, see TP_F_FP8_HILO) runs as
+                                     ONE persistent launch: the column-parallel items, then the
+                                     row-parallel items, each of which waits only for its own shard's
+                                     first half; the last shard of each 128-row output tile folds the t
+                                     partials in shard order (for bf16 weights, the same bits as the
+                                     split path) */
 
 /* Size in bytes of the packed buffer for (shape, kind); 0 if the shape is invalid. */
 size_t tp_packed_bytes(const tp_shape* shape /* host */, int32_t kind);
