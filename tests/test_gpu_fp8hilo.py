@@ -1,4 +1,4 @@
-"""Split activations on the e4m3-weight decode block (TP_F_FP8_HILO): one persistent tcgen05
+"""Hi/lo activation codes on the e4m3-weight decode block (TP_F_FP8_HILO, the default): one persistent tcgen05
 launch per block that splits each bf16 activation exactly into two e4m3 codes, x / s = hi + lo
 with s a power of two per token, and multiplies e4m3 x e4m3 (kind::f8f6f4) with the weights
 taken from shared memory as they landed.  The numeric reading is the default one (bf16
@@ -36,16 +36,16 @@ def dev():
 
 
 @pytest.mark.parametrize("t,M", [(1, 16), (2, 5), (4, 64), (8, 16), (8, 1), (2, 33)])
-def test_split_blocks_vs_oracle(dev, t, M):
+def test_hilo_blocks_vs_oracle(dev, t, M):
     m = Mlp(2048, 7168, t, M, dev, seed=23, wtype=FP8)
     for res in (True, False):
         y, h = m.run(residual=res, flags=SPL)
         y_ref, h_ref = m.oracle(residual=res)
-        check_close(bits(y), y_ref, what=f"split MLP t={t} M={M} res={res}")
-        check_h(bits(h), h_ref, what=f"split h t={t} M={M}")
+        check_close(bits(y), y_ref, what=f"hilo MLP t={t} M={M} res={res}")
+        check_h(bits(h), h_ref, what=f"hilo h t={t} M={M}")
     qkv, qkv_ref, y, y_ref = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=24, flags=SPL)
-    check_close(bits(qkv), qkv_ref, what=f"split qkv t={t} M={M}")
-    check_close(bits(y), y_ref, what=f"split o_proj t={t} M={M}")
+    check_close(bits(qkv), qkv_ref, what=f"hilo qkv t={t} M={M}")
+    check_close(bits(y), y_ref, what=f"hilo o_proj t={t} M={M}")
 
 
 def close_to(a, b, what):
@@ -60,19 +60,19 @@ def close_to(a, b, what):
 
 
 @pytest.mark.parametrize("t,M", [(2, 16), (8, 48)])
-def test_split_agrees_with_widening_block(dev, t, M):
+def test_hilo_agrees_with_widening_block(dev, t, M):
     m = Mlp(2048, 7168, t, M, dev, seed=25, wtype=FP8)
     ys, hs = m.run(flags=SPL)
     yw, hw = m.run(flags=TC)
-    close_to(hs, hw, f"h split vs widened t={t} M={M}")
-    close_to(ys, yw, f"y split vs widened t={t} M={M}")
+    close_to(hs, hw, f"h hilo vs widened t={t} M={M}")
+    close_to(ys, yw, f"y hilo vs widened t={t} M={M}")
     qs, _, ps, _ = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=26, flags=SPL)
     qw, _, pw, _ = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=26, flags=TC)
-    close_to(qs, qw, f"qkv split vs widened t={t} M={M}")
-    close_to(ps, pw, f"o_proj split vs widened t={t} M={M}")
+    close_to(qs, qw, f"qkv hilo vs widened t={t} M={M}")
+    close_to(ps, pw, f"o_proj hilo vs widened t={t} M={M}")
 
 
-def test_split_token_magnitudes(dev):
+def test_hilo_token_magnitudes(dev):
     """Every token has its own power-of-two scale: rows 2^-24 .. 2^24 apart, a zero row, a row
     with one outlier, must each meet the bar on their own."""
     t, M, d, ffn = 2, 16, 1024, 4096
@@ -88,23 +88,23 @@ def test_split_token_magnitudes(dev):
         if i == 13:
             assert torch.all(y[i] == 0) and torch.all(h[i] == 0)
             continue
-        check_close(bits(y[i:i + 1]), y_ref[i:i + 1], what=f"split y, token {i}")
-        check_h(bits(h[i:i + 1]), h_ref[i:i + 1], what=f"split h, token {i}")
+        check_close(bits(y[i:i + 1]), y_ref[i:i + 1], what=f"hilo y, token {i}")
+        check_h(bits(h[i:i + 1]), h_ref[i:i + 1], what=f"hilo h, token {i}")
 
 
 @pytest.mark.parametrize("t", [1, 8])
-def test_split_70b_blocks_vs_oracle(dev, t):
+def test_hilo_70b_blocks_vs_oracle(dev, t):
     m = Mlp(8192, 28672, t, 16, dev, seed=28, wtype=FP8)
     y, h = m.run(flags=SPL)
     y_ref, h_ref = m.oracle()
-    check_close(bits(y), y_ref, what=f"split 70B MLP t={t}")
-    check_h(bits(h), h_ref, what=f"split 70B h t={t}")
+    check_close(bits(y), y_ref, what=f"hilo 70B MLP t={t}")
+    check_h(bits(h), h_ref, what=f"hilo 70B h t={t}")
     qkv, qkv_ref, y, y_ref = _fp8_proj(8192, 64, 8, 128, t, 16, dev, seed=29, flags=SPL)
-    check_close(bits(qkv), qkv_ref, what=f"split 70B qkv t={t}")
-    check_close(bits(y), y_ref, what=f"split 70B o_proj t={t}")
+    check_close(bits(qkv), qkv_ref, what=f"hilo 70B qkv t={t}")
+    check_close(bits(y), y_ref, what=f"hilo 70B o_proj t={t}")
 
 
-def test_split_repeats_bitwise_with_one_shared_workspace(dev):
+def test_hilo_repeats_bitwise_with_one_shared_workspace(dev):
     """Split and widening blocks of several token counts, MLP and attention, interleaved on one
     workspace with overlapping launches: every repeat gives the same bits."""
     d, ffn, n_q, n_kv, hd, t = 2048, 7168, 16, 8, 128, 8
@@ -142,4 +142,4 @@ def test_split_repeats_bitwise_with_one_shared_workspace(dev):
     M = Ms[-1]
     deq = [O.dequantize_fp8(*O.quantize_fp8_per_channel(O.as_f64(bits(w)))) for w in (wqkv, wo)]
     y_ref, _ = O.proj(bits(xs[M]), deq[0], deq[1], n_q, n_kv, hd, residual=bits(xs[M]))
-    check_close(bits(first[-1][0]), y_ref, what="shared-workspace split proj")
+    check_close(bits(first[-1][0]), y_ref, what="shared-workspace hilo proj")
