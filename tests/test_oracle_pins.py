@@ -250,6 +250,52 @@ def test_fp8_exact_values_round_trip():
     assert np.array_equal(O.dequantize_fp8(q, s), w.astype(np.float64))
 
 
+def test_colpar_scales_layout_by_hand():
+    """Packed-row scales of column-parallel FP8 shards, listed by hand.  Gate scales are
+    100 + n and up scales 200 + n, so a swap of gate and up, or of two 8-feature blocks,
+    changes the list.  ffn = 32, t = 2: each shard owns 16 features, packed as
+    [8 gate | 8 up | 8 gate | 8 up]."""
+    s_gate = np.arange(32, dtype=np.float32) + 100
+    s_up = np.arange(32, dtype=np.float32) + 200
+    got = O.colpar_scales([s_gate, s_up], "gate_up", 2, ffn=32)
+    want0 = list(range(100, 108)) + list(range(200, 208)) + list(range(108, 116)) + list(range(208, 216))
+    want1 = list(range(116, 124)) + list(range(216, 224)) + list(range(124, 132)) + list(range(224, 232))
+    assert [list(map(int, g)) for g in got] == [want0, want1]
+    assert all(g.dtype == np.float32 for g in got)
+    # QKV: 4 q heads, 2 kv heads of 2 columns (q 0..7, k 8..11, v 12..15), t = 2, scale 10 + column:
+    # shard 0 holds q heads 0,1, k head 0, v head 0; shard 1 the rest
+    sq = np.arange(16, dtype=np.float32) + 10
+    got = O.colpar_scales([sq], "qkv", 2, n_q=4, n_kv=2, hd=2)
+    assert [list(map(int, g)) for g in got] == [[10, 11, 12, 13, 18, 19, 22, 23],
+                                                [14, 15, 16, 17, 20, 21, 24, 25]]
+
+
+# The FP8 quantisers divide in IEEE binary32.  A hand case where that differs from a float64
+# divide: a column (or row) [a, w] with a = 43 * 2^-12 = 0.010498046875 and w = 3a/4 =
+# 0.00787353515625, both bf16 values.  s = binary32(a / 448) lies just below a / 448 (43/1835008
+# is not a binary32 value), so the exact quotient w / s is a little above 336 = 448 * 3/4, while
+# the binary32 quotient rounds to 336.0 exactly.  336 is the midpoint between the e4m3 values
+# 320 (1.010b * 2^8, code 0x7A) and 352 (1.011b * 2^8, code 0x7B): ties go to the even mantissa,
+# 320, whereas the float64 quotient rounds up to 352.
+_DIV_A, _DIV_W = 43 * 2.0 ** -12, 0.75 * 43 * 2.0 ** -12
+
+
+def test_fp8_division_is_binary32_by_hand():
+    from fractions import Fraction
+    s = np.float32(np.float32(_DIV_A) / np.float32(448.0))
+    assert Fraction(float(s)) < Fraction(43, 1835008)                 # s rounded down
+    assert Fraction(_DIV_W) / Fraction(float(s)) > 336                 # exact quotient above the tie
+    assert np.float32(_DIV_W) / s == np.float32(336.0)                 # binary32 quotient on the tie
+    col = np.array([[_DIV_A], [_DIV_W]], dtype=np.float32)
+    q, sc = O.quantize_fp8_per_channel(col)
+    assert sc[0] == s and list(q[:, 0]) == [0x7E, 0x7A]
+    q, sc = O.quantize_fp8_per_token(col.T)
+    assert sc[0] == s and list(q[0, :]) == [0x7E, 0x7A]
+    # the same pair with the sign flipped: codes 0xFE, 0xFA
+    q, _ = O.quantize_fp8_per_channel(-col)
+    assert list(q[:, 0]) == [0xFE, 0xFA]
+
+
 # ---------------------------------------------------------------- accounting printed on the pages
 
 
