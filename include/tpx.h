@@ -138,10 +138,13 @@ typedef struct {
                                      the token's row of x, or its shard's columns of h / o_in) and
                                      multiplies e4m3 x e4m3, the weights straight from shared memory.
                                      This is what those blocks run by default (the flag also overrides
-                                     TP_F_KERNEL_TC).  The numeric reading is unchanged (bf16 activations
-                                     times the e4m3 weights, fp32 sums, in another order); activations
-                                     below 2^-10 of the token's largest lose their lowest bits.  No
-                                     effect on bf16 weights or where the one-launch block does not apply */
+                                     TP_F_KERNEL_TC).  The split is exact for every activation of at
+                                     least 2^-10 of its token's largest (2^-2 of the scaled range): those
+                                     are multiplied as the bf16 values they are.  A smaller activation
+                                     loses the bits below 2^-17 of the token's largest, so the result
+                                     approximates the bf16-activation product (fp32 sums, in another
+                                     order) rather than equalling it.  No effect on bf16 weights or where
+                                     the one-launch block does not apply */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, 128-row tiles; k %
                                      64 for bf16 weights, k % 128 for e4m3, see TP_F_FP8_HILO) runs as
@@ -159,7 +162,8 @@ tp_status tp_describe(const tp_shape* shape /* host */, int32_t kind, tp_packed_
 
 /* Split and pack an unsharded weight for degree t (column split on the output dim for
  * GATE_UP/QKV, row split on the input dim for DOWN/O; "ColumnParallelLinear" /
- * "RowParallelLinear", scalablesystem.dev).  W0: [in,out] bf16 (W_gate for GATE_UP);
+ * "RowParallelLinear", scalablesystem.dev "The Tensor-Parallel Shard Group").  A set-up call,
+ * not on the forward path: it is the one entry point that synchronises its stream.  W0: [in,out] bf16 (W_gate for GATE_UP);
  * W1: W_up for GATE_UP, else NULL.  packed: packed_bytes >= tp_packed_bytes().
  * Writes the layout described above; for FP8 also quantises (shape.wtype).  Fills
  * *desc_out (host).  Synchronises `stream` before returning, so the packed buffer is
@@ -174,11 +178,12 @@ tp_status tp_partition_weights(const tp_shape* shape /* host */, int32_t kind, c
 size_t tp_workspace_bytes(const tp_shape* shape /* host */, int32_t M, uint32_t flags);
 
 /* SwiGLU MLP block: h = silu(x Wg) * (x Wu) column-parallel per shard, then
- * y = fold_s(h_s Wd_s) + residual row-parallel ("gate_proj and up_proj are
- * column-parallel ... down_proj is row-parallel", scalablesystem.dev).
- * x, residual (nullable): [M, d] bf16; y: [M, d] bf16; h_out: [M, ffn] bf16 scratch for
- * h, required (it is the activation between the two halves, shard s owns columns
- * [s*F_s, (s+1)*F_s)).  M == 0 returns TP_OK with no work.  y may alias residual. */
+ * y = fold_s(h_s Wd_s) + residual row-parallel (scalablesystem.dev "The Tensor-Parallel Shard
+ * Group": the MLP's gate and up projections column-parallel, its down projection row-parallel).
+ * x, residual (nullable): [M, d] bf16; y: [M, d] bf16; h_out: [M, ffn] bf16, required: it is
+ * where the column-parallel half leaves h for the row-parallel half (the library allocates
+ * nothing, so the caller owns that buffer), and it holds h afterwards, shard s's columns at
+ * [s*F_s, (s+1)*F_s).  M == 0 returns TP_OK with no work.  y may alias residual. */
 tp_status tp_mlp_forward(const tp_packed_desc* gu /* host */, const void* gu_w,
                          const tp_packed_desc* dn /* host */, const void* dn_w, const void* x,
                          const void* residual, int32_t M, void* y, void* h_out, void* ws,
@@ -188,7 +193,8 @@ tp_status tp_mlp_forward(const tp_packed_desc* gu /* host */, const void* gu_w,
  * o_in = local attention per shard; y = fold_s(o_in_s Wo_s) + residual row-parallel
  * ("TPAttentionBlock", scalablesystem.dev).  The attention core is a one-token
  * context: every q head returns the v of its kv group.  qkv_out: [M, (n_q+2n_kv)hd]
- * bf16, shard-major (shard s = [q_s | k_s | v_s]); o_in: [M, n_q*hd] bf16 scratch. */
+ * bf16, shard-major (shard s = [q_s | k_s | v_s]); o_in: [M, n_q*hd] bf16, required: the
+ * attention output that the row-parallel o_proj reads (caller-owned, as h_out above). */
 tp_status tp_proj_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
                           const tp_packed_desc* o /* host */, const void* o_w, const void* x,
                           const void* residual, int32_t M, void* y, void* qkv_out, void* o_in,
@@ -199,7 +205,12 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv /* host */, const void* qkv_
  * with RMSNorm eps, gain 1.  The four packed weights must describe one block (same d, t,
  * dtype; heads for QKV/O, ffn for GATE_UP/DOWN).  x, y: [M, d] bf16 (y may alias x).
  * scratch: tp_layer_scratch_bytes(shape, M) bytes of device memory for the activations
- * between the steps (normed inputs, h1, qkv, attention output, h); ws as for the blocks. */
+ * between the steps; ws as for the blocks.  With B = round_up(M*d*2, 256) the scratch holds,
+ * in bf16, a [M, d] at 0, h1 [M, d] at B, the attention output [M, n_q*hd] at 2B, b [M, d] at
+ * 3B, qkv [M, (n_q+2n_kv)hd] (shard-major) at 4B and h [M, ffn] at 4B + round_up(M*Q*2, 256);
+ * after the call h1, the attention output, qkv and h hold this layer's values.  At decode token
+ * counts the norms are folded into the two block launches (per-token factors on the
+ * column-parallel accumulators) and a, b are not written. */
 size_t tp_layer_scratch_bytes(const tp_shape* shape /* host */, int32_t M);
 tp_status tp_layer_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
                            const tp_packed_desc* o /* host */, const void* o_w,
@@ -215,14 +226,18 @@ tp_status tp_layer_forward(const tp_packed_desc* qkv /* host */, const void* qkv
 tp_status tp_reduce_partials(const float* partials, int32_t t, int32_t M, int32_t d,
                              const void* residual, void* y, void* stream);
 
-/* Column-parallel building block: out[m][s*rows + r] for every shard s and packed row r.
+/* Column-parallel building block ("ColumnParallelLinear.forward", scalablesystem.dev "The
+ * Tensor-Parallel Shard Group"; A = [A_1 | ... | A_t], each shard's output a slice of the
+ * features, arunshar.com ch. 12 "Tensor Parallelism (Megatron-Style)"):
+ * out[m][s*rows + r] for every shard s and packed row r.
  * GATE_UP: out = h [M, ffn] bf16 (SwiGLU applied);  QKV: out = qkv [M, Q] bf16.
  * With TP_F_FP32_COLPAR_OUT (QKV only) out is fp32.  ws is optional (NULL, or a workspace of
  * tp_workspace_bytes(shape, M) bytes, which lets the tcgen05 kernel balance work across SMs). */
 tp_status tp_colpar_forward(const tp_packed_desc* desc /* host */, const void* w, const void* x,
                             int32_t M, void* out, void* ws, size_t ws_bytes, uint32_t flags, void* stream);
 
-/* Row-parallel building block without the fold: partials[s][m][n] = (a_s W_s)[m][n],
+/* Row-parallel building block without the fold (the shard partials Z_s of arunshar.com ch. 12
+ * "Tensor Parallelism (Megatron-Style)", before their sum): partials[s][m][n] = (a_s W_s)[m][n],
  * a_s = columns [s*K_s, (s+1)*K_s) of a [M, t*K_s] bf16; partials [t][M][N] fp32. */
 tp_status tp_rowpar_partials(const tp_packed_desc* desc /* host */, const void* w, const void* a,
                              int32_t M, float* partials, void* stream);
@@ -248,7 +263,10 @@ tp_status tp_rowpar_forward(const tp_packed_desc* desc /* host */, const void* w
  * device current), so make that first call before any stream capture.  Every call on a
  * device shares the one array and leaves its contents behind (the tickets are cleared
  * at the start of each call): calls that may overlap on the GPU (other streams, other
- * threads) race and must be serialised by the caller. */
+ * threads) race and must be serialised by the caller.  TP_F_FP8_ACT is refused
+ * (TP_ERR_UNSUPPORTED): its quantised activations have no room in the array.  The resolved
+ * address belongs to the device's current context: after a cudaDeviceReset this entry point,
+ * like the rest of the library, must not be called again in the same process. */
 tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc /* host */, const void* w, const void* a,
                                     const void* residual, int32_t M, void* y, uint32_t flags,
                                     void* stream);
@@ -319,7 +337,9 @@ tp_status tp_embed_lookup(const tp_packed_desc* desc /* host */, const void* w, 
  * divide).  q: [M, K] bytes; s: [M] fp32 (device).  K % 8 == 0; pointers 16-byte aligned. */
 tp_status tp_quantize_fp8_per_token(const void* x, int32_t M, int32_t K, void* q, float* s, void* stream);
 
-/* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g). */
+/* RMSNorm over the hidden dim, gain 1 (or gain [d] bf16): out = bf16(x / sqrt(mean(x^2) + eps) * g).
+ * The norm that the layer applies, replicated, to its full hidden vector between the
+ * reductions (arunshar.com ch. 12, "12.3.1 Sequence Parallelism for LayerNorm and Dropout"). */
 tp_status tp_rmsnorm(const void* x, const void* gain, float eps, int32_t M, int32_t d, void* out,
                      void* stream);
 

@@ -1036,6 +1036,8 @@ extern "C" tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc, const
   if (st != TP_OK) return st;
   if ((flags & ~kFwdFlags) || bad_kernel_flags(flags))
     return TP_ERR_INVALID_ARG;
+  // the per-token e4m3 activations would need a region of their own in the array
+  if (flags & TP_F_FP8_ACT) return TP_ERR_UNSUPPORTED;
   if (M < 0 || (M > 0 && (!a || !y))) return TP_ERR_INVALID_ARG;
   if (M == 0) return TP_OK;
   if (!aligned16(a) || !aligned16(y) || (residual && !aligned16(residual))) return TP_ERR_ALIGN;

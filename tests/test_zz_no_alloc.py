@@ -56,12 +56,45 @@ def test_noalloc_matches_workspace_entry_point_twice(dev, d, ffn, t, M, flags):
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))   # same kernels, same bits
 
 
+@pytest.mark.parametrize("kind,M", [(tpx.TP_W_O, 16), (tpx.TP_W_DOWN, 16), (tpx.TP_W_DOWN, 5)])
+def test_noalloc_e4m3_weights_match_workspace_entry_point_twice(dev, kind, M):
+    """e4m3 weights at decode token counts run the TMA-fed kernel, which keeps its work pieces
+    in the balancing scratch and its counters in the ticket words of the static array: two calls
+    in a row, each bit-equal to the workspace entry point."""
+    d, ffn, n_q, n_kv, hd, t = 8192, 28672, 64, 8, 128, 8
+    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=tpx.TP_FP8_E4M3)
+    K = ffn if kind == tpx.TP_W_DOWN else n_q * hd
+    wt = inputs.normal_bf16((K, d), 0.02, 0, inputs.STREAM_W_DOWN, dev)
+    w, desc = tpx.tp_partition_weights(sh, kind, wt)
+    del wt
+    ws = tpx.new_workspace(sh, M, dev)
+    for call in range(2):
+        a = inputs.normal_bf16((M, K), 1.0, call, 33, dev)
+        res = inputs.normal_bf16((M, d), 1.0, call, 34, dev)
+        y_ref = torch.empty((M, d), dtype=torch.bfloat16, device=dev)
+        tpx.tp_rowpar_forward(desc, w, a, res, y_ref, ws)
+        y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device=dev)
+        tpx.tp_rowpar_forward_noalloc(desc, w, a, res, y)
+        assert tpx.tp_sync(timeout_ms=20000) == tpx.TP_OK
+        assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
 def test_noalloc_rejects_requests_beyond_its_scratch(dev):
     cap = tpx.tp_noalloc_scratch_capacity()
     assert cap == 32 << 20
-    # 405B-shaped o_proj at 64 tokens needs 8 * 64 * 16384 * 4 bytes of partials: 32 MiB + more
+    # 405B-shaped o_proj at 64 tokens needs 8 * 64 * 16384 * 4 bytes of partials: 32 MiB + more.
+    # Real (small) device buffers stand in for the operands: the call must return before it
+    # touches them, and if it ever did not, it would still touch only memory of this process.
     sh = tpx.make_shape(16384, n_q=128, n_kv=8, hd=128, t=8)
     desc = tpx.tp_describe(sh, tpx.TP_W_O)
-    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: the size check fails first
-    st = tpx.lib().tp_rowpar_forward_noalloc(ctypes.byref(desc), fake, fake, None, 64, fake, 0, None)
+    buf = torch.zeros(4096, dtype=torch.uint8, device=dev)
+    p = ctypes.c_void_p(buf.data_ptr())
+    st = tpx.lib().tp_rowpar_forward_noalloc(ctypes.byref(desc), p, p, None, 64, p, 0, None)
     assert st == tpx.TP_ERR_WORKSPACE
+    # the quantised-activation path needs scratch this entry point does not hold: refused up front
+    sh8 = tpx.make_shape(256, ffn=1024, t=2, wtype=tpx.TP_FP8_E4M3)
+    desc8 = tpx.tp_describe(sh8, tpx.TP_W_DOWN)
+    st = tpx.lib().tp_rowpar_forward_noalloc(ctypes.byref(desc8), p, p, None, 8, p, tpx.TP_F_FP8_ACT, None)
+    assert st == tpx.TP_ERR_UNSUPPORTED
+    assert tpx.tp_sync(timeout_ms=10000) == tpx.TP_OK
+    assert int(buf.count_nonzero()) == 0
