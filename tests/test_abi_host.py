@@ -96,7 +96,7 @@ def _call_mlp(gu, dn, M=8, flags=0, ws=FAKE, ws_bytes=1 << 30):
 
 
 def test_wrong_shard_layout_is_rejected():
-    """A packed buffer for another t (the 'fluent, plausible, wrong output' of loading the
+    """A packed buffer for another t (the believable but wrong output of loading the
     wrong shard, scalablesystem.dev 'The Checkpoint Loader') must not run."""
     gu = tpx.tp_describe(tpx.make_shape(4096, ffn=14336, t=8), tpx.TP_W_GATE_UP)
     dn4 = tpx.tp_describe(tpx.make_shape(4096, ffn=14336, t=4), tpx.TP_W_DOWN)

@@ -92,16 +92,16 @@ def test_hilo_token_magnitudes(dev):
         check_h(bits(h[i:i + 1]), h_ref[i:i + 1], what=f"hilo h, token {i}")
 
 
-@pytest.mark.parametrize("t", [1, 8])
-def test_hilo_70b_blocks_vs_oracle(dev, t):
-    m = Mlp(8192, 28672, t, 16, dev, seed=28, wtype=FP8)
+@pytest.mark.parametrize("t,M", [(1, 16), (8, 16), (8, 4)])
+def test_hilo_70b_blocks_vs_oracle(dev, t, M):
+    m = Mlp(8192, 28672, t, M, dev, seed=28, wtype=FP8)
     y, h = m.run(flags=SPL)
     y_ref, h_ref = m.oracle()
-    check_close(bits(y), y_ref, what=f"hilo 70B MLP t={t}")
-    check_h(bits(h), h_ref, what=f"hilo 70B h t={t}")
-    qkv, qkv_ref, y, y_ref = _fp8_proj(8192, 64, 8, 128, t, 16, dev, seed=29, flags=SPL)
-    check_close(bits(qkv), qkv_ref, what=f"hilo 70B qkv t={t}")
-    check_close(bits(y), y_ref, what=f"hilo 70B o_proj t={t}")
+    check_close(bits(y), y_ref, what=f"hilo 70B MLP t={t} M={M}")
+    check_h(bits(h), h_ref, what=f"hilo 70B h t={t} M={M}")
+    qkv, qkv_ref, y, y_ref = _fp8_proj(8192, 64, 8, 128, t, M, dev, seed=29, flags=SPL)
+    check_close(bits(qkv), qkv_ref, what=f"hilo 70B qkv t={t} M={M}")
+    check_close(bits(y), y_ref, what=f"hilo 70B o_proj t={t} M={M}")
 
 
 def test_hilo_repeats_bitwise_with_one_shared_workspace(dev):

@@ -85,8 +85,11 @@ def test_fused_proj_exact_on_integers(dev, t, M):
     assert np.array_equal(y, y_ref)
 
 
-def test_fused_proj_70b_shape_exact_on_integers(dev):
-    qkv, qkv_ref, o_in, o_ref, y, y_ref = _proj_int_case(8192, 64, 8, 128, 8, 16, dev, lo=-1, hi=1)
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_fused_proj_70b_shape_exact_on_integers(dev, M):
+    """The 70B attention block (80 QKV tiles, 512 o_proj tiles) at one, eight and sixteen tokens:
+    qkv, the attention stand-in and y bit-exact on small integers."""
+    qkv, qkv_ref, o_in, o_ref, y, y_ref = _proj_int_case(8192, 64, 8, 128, 8, M, dev, lo=-1, hi=1)
     assert np.array_equal(qkv, qkv_ref)
     assert np.array_equal(o_in, o_ref)
     assert np.array_equal(y, y_ref)

@@ -1,7 +1,7 @@
 """GPU parity: the CUDA path through the C ABI against the float64 CPU oracle.
 
 Bars (per the tensor-parallel split-vs-unsplit equivalence the pages ask for, checked
-"to floating-point tolerance", engineer-atlas.dev 'What must stay true after deployment'):
+equal up to floating-point rounding, engineer-atlas.dev 'What must stay true after deployment'):
 relative Frobenius error <= 5e-3 and max |err| <= 2e-2 * RMS(y) for bf16 weights; 3e-2
 relative Frobenius for FP8 weights against the oracle on the dequantised weights.
 Integer, byte and layout work (packing, quantisation codes, exact-integer products,

@@ -147,9 +147,9 @@ def test_tc_streamk_rowpar_exact_on_integers(dev, t, M):
 # ---------------------------------------------------------------- full-size configurations
 
 
-def _layer(dev, M, t=8, d=8192, ffn=28672, n_q=64, n_kv=8, hd=128, seed=0):
+def _layer(dev, M, t=8, d=8192, ffn=28672, n_q=64, n_kv=8, hd=128, seed=0, wtype=tpx.TP_BF16):
     """A 70B-shaped layer's linear parts through the public entry points, as the bench runs it."""
-    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t)
+    sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=wtype)
     x, wg, wu, wd = inputs.mlp_inputs(d, ffn, M, seed=seed, device=dev)
     _, wqkv, wo = inputs.proj_inputs(d, n_q, n_kv, hd, 1, seed=seed, device=dev)
     gu_w, gu = tpx.tp_partition_weights(sh, tpx.TP_W_GATE_UP, wg, wu)
@@ -194,6 +194,28 @@ def test_70b_layer_prefill_sampled_rows(dev):
     check_close(y1b, y1_ref, what="70B attention block, prefill rows")
     y_ref, _ = O.mlp(y1b, bits(wg), bits(wu), bits(wd), residual=y1b)
     check_close(bits(y)[rows], y_ref, what="70B MLP block, prefill rows")
+    assert not torch.isnan(y).any() and not torch.isnan(y1).any()
+
+
+def test_70b_fp8_layer_prefill_sampled_rows(dev):
+    """70B-shaped layer with e4m3 weights at prefill M=8192, t=8, in the launch configuration
+    the bench times (each weight widened once into the workspace's bf16 scratch, 0.94 GB for
+    the gate/up weight, then the tcgen05 GEMM with the per-channel scales in its epilogue).
+    Sampled rows over every token tile, against the oracle on the dequantised weights."""
+    M = 8192
+    x, y1, y, ws_list, (n_q, n_kv, hd) = _layer(dev, M, wtype=tpx.TP_FP8_E4M3)
+    deq = []
+    for w in ws_list:
+        q, s = O.quantize_fp8_per_channel(O.as_f64(bits(w)))
+        deq.append(O.dequantize_fp8(q, s))
+        del q
+    wqkv, wo, wg, wu, wd = deq
+    rows = np.array([0, 1, 127, 128, 255, 256, 1000, 4095, 4096, 6143, 8190, 8191])
+    xb, y1b = bits(x)[rows], bits(y1)[rows]
+    y1_ref, _ = O.proj(xb, wqkv, wo, n_q, n_kv, hd, residual=xb)
+    check_close(y1b, y1_ref, what="70B fp8 attention block, prefill rows")
+    y_ref, _ = O.mlp(y1b, wg, wu, wd, residual=y1b)
+    check_close(bits(y)[rows], y_ref, what="70B fp8 MLP block, prefill rows")
     assert not torch.isnan(y).any() and not torch.isnan(y1).any()
 
 
