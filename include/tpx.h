@@ -61,8 +61,8 @@ typedef enum {
 } tp_wkind;
 
 /* Model dims and the shard count.  ffn is used by GATE_UP/DOWN, the head dims by
- * QKV/O, vocab by VOCAB/EMBED.  t must be 1, 2, 4 or 8 and divide ffn, n_q and n_kv ("TP
- * degree must divide the KV heads"; t > n_kv head replication is not supported).  The
+ * QKV/O, vocab by VOCAB/EMBED.  t must be 1, 2, 4 or 8 and divide ffn, n_q and n_kv (a GQA
+ * head cannot be split between shards; t > n_kv head replication is not supported).  The
  * vocabulary is padded with zero rows so that each shard holds a multiple of 128 ids:
  * vocab_padded = round_up(vocab, 128 t), V_s = vocab_padded / t ids per shard. */
 typedef struct {
@@ -275,8 +275,8 @@ tp_status tp_rowpar_forward_noalloc(const tp_packed_desc* desc /* host */, const
 size_t tp_noalloc_scratch_capacity(void);
 
 /* Decode attention over a KV cache, head-sharded (each shard attends with its own q heads over
- * the cache of its own kv heads, whole GQA groups, "local attention over this GPU's heads",
- * scalablesystem.dev "The Tensor-Parallel Shard Group"; "the KV cache splits too", vidyal.ai).
+ * the cache of its own kv heads, whole GQA groups: each shard attends with its own heads,
+ * scalablesystem.dev "The Tensor-Parallel Shard Group", and the KV cache is split with them, vidyal.ai). 
  * One new token per sequence m: its k and v (from qkv) are first written into the cache at
  * position lens[m]; then, for q head h and its kv head g = h / (n_q / n_kv),
  *   o_in[m][h*hd + i] = bf16( sum_j softmax_j(q . k_j / sqrt(hd)) v_j[i] ),  j = 0 .. lens[m],

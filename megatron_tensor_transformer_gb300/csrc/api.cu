@@ -395,8 +395,10 @@ tp_status x8_setup(TcArgs& a, const tp_packed_desc* d, const void* w, const bf16
 }
 
 // Column-parallel half over token blocks of at most 64 (skinny) or all tokens (tcgen05).
+// in_scale (nullable, tcgen05 path only): per-token factors on the accumulators (a folded RMSNorm).
 tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int M, void* out,
-                     int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr, size_t ws_bytes = 0) {
+                     int mode, cudaStream_t st, uint32_t flags = 0, void* sk_ws = nullptr, size_t ws_bytes = 0,
+                     const float* in_scale = nullptr) {
   const int t = d->shape.t;
   const int rows = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const int ldo = mode == COLPAR_SWIGLU ? rows / 2 * t : rows * t;
@@ -432,9 +434,11 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
     a.M = M;
     a.out = out;
     a.ldo = ldo;
+    a.tok_scales = in_scale;
     set_streamk(a, sk_ws);
     return launch_tc(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
   }
+  if (in_scale) return TP_ERR_UNSUPPORTED;
   if ((mode == COLPAR_BF16 || mode == COLPAR_SWIGLU) &&
       pick_ring(flags, d, rows, K, M, false, sk_ws, ws_bytes)) {
     RingArgs r = ring_args(d, w, rows, K, x, K, M, sk_ws);
@@ -467,9 +471,11 @@ tp_status run_colpar(const tp_packed_desc* d, const void* w, const bf16* x, int 
 
 // Row-parallel half: partials_user != NULL -> write [t][M][N] partials only; otherwise fold
 // (in the CTA, by ticket, or unfused through tp_reduce_partials) into y with the residual.
+// norm_ss (nullable, the chained tcgen05 path only): per (token, 32-row group) sums of squares of
+// the stored y, for the next RMSNorm.
 tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, int M,
                      const bf16* res, bf16* y, float* partials_user, void* ws, size_t ws_bytes,
-                     uint32_t flags, cudaStream_t st) {
+                     uint32_t flags, cudaStream_t st, float* norm_ss = nullptr) {
   const int t = d->shape.t;
   const int N = (int)d->rows_per_shard, K = (int)d->k_per_shard;
   const RowparPlan plan = rowpar_plan(N, t);
@@ -519,8 +525,11 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
       a.y = y;
       a.partials = partials_user;
       a.pM = M;
+      if (norm_ss && (partials_user || N % 32 != 0)) return TP_ERR_UNSUPPORTED;
+      a.norm_ss = norm_ss;
       return launch_tc(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
     }
+    if (norm_ss) return TP_ERR_UNSUPPORTED;
     for (int m0 = 0; m0 < M; m0 += kSkinnyMaxM) {  // per-shard partials in the workspace
       const int mb = M - m0 < kSkinnyMaxM ? M - m0 : kSkinnyMaxM;
       a.mode = TC_ROWPAR_SHARD;
@@ -540,6 +549,7 @@ tp_status run_rowpar(const tp_packed_desc* d, const void* w, const bf16* a_in, i
     }
     return TP_OK;
   }
+  if (norm_ss) return TP_ERR_UNSUPPORTED;
   if (ring) {
     RingArgs r = ring_args(d, w, N, K, a_in, K * t, M, ws);
     if (!r.err) return TP_ERR_CUDA;
@@ -652,6 +662,18 @@ bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {
   if (a.d != b.d || a.t != b.t || a.wtype != b.wtype) return false;
   if (mlp) return a.ffn == b.ffn;
   return a.n_q_heads == b.n_q_heads && a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim;
+}
+
+// A prefill layer whose four GEMMs all run on the tcgen05 path, with the chained row-parallel
+// fold (no flag asking for anything else): the RMSNorms fold into their epilogues.
+bool prefill_fold(uint32_t flags, const tp_packed_desc* q, const tp_packed_desc* o, const tp_packed_desc* gu,
+                  const tp_packed_desc* dn, int M) {
+  if (M <= kFusedMaxM || (flags & (TP_F_FP8_ACT | TP_F_SPLIT_BLOCK | TP_F_KERNEL_SKINNY | TP_F_UNFUSED_REDUCE)))
+    return false;
+  if (q->shape.d % 32 != 0) return false;
+  for (const tp_packed_desc* d : {q, o, gu, dn})
+    if (!pick_tc(flags, (int)d->rows_per_shard, (int)d->k_per_shard, d->wtype == TP_FP8_E4M3, M)) return false;
+  return true;
 }
 
 }  // namespace
@@ -838,6 +860,43 @@ tp_status tp_layer_forward(const tp_packed_desc* qkv, const void* qkv_w, const t
     return run_fused(FUSED_MLP, gu, gu_w, dn, dn_w, static_cast<const bf16*>(h1), static_cast<const bf16*>(h1), M,
                      static_cast<bf16*>(y), static_cast<bf16*>(h), static_cast<bf16*>(h), ws, flags, s, r_h1, 0,
                      nullptr, eps);
+  }
+  if (prefill_fold(flags, qkv, o, gu, dn, M)) {
+    // Prefill: the RMSNorms as per-token factors on the column-parallel GEMMs' accumulators.  The
+    // factors of x come from one pass over x; the o_proj epilogue, which writes h1, also leaves
+    // h1's sums of squares per 32-row group, summed in order into h1's factors.  The normalised
+    // activations are never written (their room in the scratch holds the sums and the factors).
+    tp_status st = check_desc(qkv, TP_W_QKV, qkv_w);
+    if (st == TP_OK) st = check_desc(o, TP_W_O, o_w);
+    if (st == TP_OK) st = check_desc(gu, TP_W_GATE_UP, gu_w);
+    if (st == TP_OK) st = check_desc(dn, TP_W_DOWN, dn_w);
+    if (st != TP_OK) return st;
+    if (!same_block(qkv->shape, o->shape, false) || !same_block(gu->shape, dn->shape, true))
+      return TP_ERR_LAYOUT_MISMATCH;
+    if ((flags & ~kFwdFlags) || bad_kernel_flags(flags)) return TP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y)) return TP_ERR_ALIGN;
+    if (!ws || ws_bytes < tp_workspace_bytes(&both, M, flags)) return TP_ERR_WORKSPACE;
+    if (!aligned16(ws)) return TP_ERR_ALIGN;
+    float* ss = static_cast<float*>(a);    // [M][d / 32] sums of squares of h1
+    float* r_x = static_cast<float*>(b);   // [M] factors of x, then [M] factors of h1
+    float* r_h1 = r_x + align_up((uint64_t)M * 4) / 4;
+    cudaStream_t s = S(stream);
+    st = cuda_status(launch_rms_factors(static_cast<const bf16*>(x), eps, M, (int)d, r_x, s));
+    if (st == TP_OK)
+      st = run_colpar(qkv, qkv_w, static_cast<const bf16*>(x), M, qk, COLPAR_BF16, s, flags, ws, ws_bytes, r_x);
+    if (st == TP_OK)
+      st = cuda_status(launch_attn1(static_cast<const bf16*>(qk), M, sa.n_q_heads, sa.n_kv_heads, sa.head_dim, sa.t,
+                                    static_cast<bf16*>(oi), s));
+    if (st == TP_OK)
+      st = run_rowpar(o, o_w, static_cast<const bf16*>(oi), M, static_cast<const bf16*>(x), static_cast<bf16*>(h1),
+                      nullptr, ws, ws_bytes, flags, s, ss);
+    if (st == TP_OK) st = cuda_status(launch_rms_factors_from_ss(ss, eps, M, (int)d, r_h1, s));
+    if (st == TP_OK)
+      st = run_colpar(gu, gu_w, static_cast<const bf16*>(h1), M, h, COLPAR_SWIGLU, s, flags, ws, ws_bytes, r_h1);
+    if (st == TP_OK)
+      st = run_rowpar(dn, dn_w, static_cast<const bf16*>(h), M, static_cast<const bf16*>(h1), static_cast<bf16*>(y),
+                      nullptr, ws, ws_bytes, flags, s);
+    return st;
   }
   tp_status st = tp_rmsnorm(x, nullptr, eps, M, (int32_t)d, a, stream);
   if (st != TP_OK) return st;

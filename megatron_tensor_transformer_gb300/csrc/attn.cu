@@ -1,7 +1,7 @@
 // Decode attention over a KV cache, head-sharded: each logical shard owns whole GQA groups (its
 // q heads and the kv heads they read) and the cache of those kv heads, so attention is local
-// to the shard ("local attention over this GPU's heads", scalablesystem.dev, "The
-// Tensor-Parallel Shard Group"; "the KV cache splits too", vidyal.ai model-parallelism).
+// to the shard: each shard attends with its own heads (scalablesystem.dev, "The
+// Tensor-Parallel Shard Group"), and the KV cache is split with them (vidyal.ai model-parallelism).
 //
 // Per sequence m (one new token each) and q head h of kv head g = h / (n_q / n_kv):
 //   o[m, h] = sum_j softmax_j(q . k_j / sqrt(hd)) v_j,   j = 0 .. len[m]

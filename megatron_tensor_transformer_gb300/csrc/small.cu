@@ -105,6 +105,62 @@ cudaError_t launch_rmsnorm(const __nv_bfloat16* x, const __nv_bfloat16* gain, fl
   return cudaGetLastError();
 }
 
+// RMSNorm as a per-token factor (the layer folds it into the next GEMM's epilogue, so the
+// normalised activations are never written): one block per token, the same sum of squares as
+// rmsnorm_kernel (eight values per thread per step, a shuffle tree per warp, then the warps in order).
+__global__ void rms_factors_kernel(const __nv_bfloat16* __restrict__ x, float eps, int d, float* __restrict__ r) {
+  __shared__ float part[32];
+  const int m = blockIdx.x;
+  const __nv_bfloat16* xr = x + (size_t)m * d;
+  float ss = 0.f;
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float a = bf16_lo(w[j]), b = bf16_hi(w[j]);
+      ss += a * a;
+      ss += b * b;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (threadIdx.x == 0) r[m] = 1.0f / sqrtf(v / (float)d + eps);
+  }
+}
+
+cudaError_t launch_rms_factors(const __nv_bfloat16* x, float eps, int M, int d, float* r, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  rms_factors_kernel<<<M, 256, 0, st>>>(x, eps, d, r);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// One thread per token: the d / 32 partial sums of squares in group order, then the factor.
+__global__ void rms_factors_from_ss_kernel(const float* __restrict__ ss, float eps, int M, int d,
+                                           float* __restrict__ r) {
+  const int m = blockIdx.x * blockDim.x + threadIdx.x;
+  if (m >= M) return;
+  const int g = d / 32;
+  const float* row = ss + (size_t)m * g;
+  float acc = 0.f;
+  for (int i = 0; i < g; ++i) acc += row[i];
+  r[m] = 1.0f / sqrtf(acc / (float)d + eps);
+}
+
+cudaError_t launch_rms_factors_from_ss(const float* ss, float eps, int M, int d, float* r, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  rms_factors_from_ss_kernel<<<(M + 127) / 128, 128, 0, st>>>(ss, eps, M, d, r);
+  note_launch();
+  return cudaGetLastError();
+}
+
 // One-token attention per shard: q head h (shard s = h / nq_s) returns the v of its kv group,
 // which lives in the same shard.  qkv is shard-major [q_s | k_s | v_s]; o_in is in head order.
 // Prefill with e4m3 weights: each shard is widened once per call, exactly, to the bf16 codes

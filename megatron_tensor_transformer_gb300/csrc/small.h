@@ -23,6 +23,10 @@ cudaError_t launch_quantize_fp8_per_token(const __nv_bfloat16* x, int ldx, int M
 // s * stride bytes, rows of d bf16), or zeros for an id outside [0, vocab).
 cudaError_t launch_embed(const uint8_t* table, uint64_t stride, int vs, int t, int vocab, int d, const int32_t* ids,
                          int M, __nv_bfloat16* x, cudaStream_t st);
+// RMSNorm (gain 1) as per-token factors: r[m] = 1/sqrt(mean_k x[m][k]^2 + eps), x [M, d] bf16.
+cudaError_t launch_rms_factors(const __nv_bfloat16* x, float eps, int M, int d, float* r, cudaStream_t st);
+// The same factors from per-(token, 32-row group) sums of squares ss [M][d / 32], summed in group order.
+cudaError_t launch_rms_factors_from_ss(const float* ss, float eps, int M, int d, float* r, cudaStream_t st);
 cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
                          __nv_bfloat16* o_in, cudaStream_t st);
 

@@ -193,9 +193,23 @@ __device__ __forceinline__ void epilogue_chunk(const TcArgs& a, int s, int p, in
 #pragma unroll
     for (int j = 0; j < 16; ++j)
       rv[j] = (a.residual && mf + j < a.M) ? __bfloat162float(a.residual[(size_t)(mf + j) * a.ldy + p]) : 0.f;
+    uint16_t yb[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (mf + j < a.M) reinterpret_cast<uint16_t*>(a.y)[(size_t)(mf + j) * a.ldy + p] = f2bf(v[j] + rv[j]);
+    for (int j = 0; j < 16; ++j) {
+      yb[j] = f2bf(v[j] + rv[j]);
+      if (mf + j < a.M) reinterpret_cast<uint16_t*>(a.y)[(size_t)(mf + j) * a.ldy + p] = yb[j];
+    }
+    if (a.norm_ss) {
+      // the warp's 32 rows of the stored values, per token: a fixed shuffle tree
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float e = __uint_as_float((uint32_t)yb[j] << 16);
+        float ss = e * e;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if ((threadIdx.x & 31) == 0 && mf + j < a.M) a.norm_ss[(size_t)(mf + j) * (a.rows / 32) + p / 32] = ss;
+      }
+    }
   }
 }
 
@@ -764,7 +778,7 @@ static cudaError_t tc_go(const TcArgs& a, cudaStream_t st, bool pdl) {
   const long long nkb_item = a.mode == TC_ROWPAR_CHAIN ? (long long)a.K / KB * a.t : a.K / KB;
   // stream-K only when whole items cannot fill the GPU: its cross-CTA fix-up costs more than
   // the imbalance of item-granular scheduling once every SM has at least one item
-  b.streamk = a.pieces && a.item_tickets && BN <= kTcStreamkMaxBN && n_items < sms &&
+  b.streamk = a.pieces && a.item_tickets && !a.norm_ss && BN <= kTcStreamkMaxBN && n_items < sms &&
               (long long)n_items * nkb_item * kTcMaxGrid < (1ll << 32);  // share table fits 32 bits
   const long long total_kb = (long long)n_items * nkb_item;
   const int grid = b.streamk ? (total_kb < sms ? (int)total_kb : sms) : (n_items < sms ? n_items : sms);

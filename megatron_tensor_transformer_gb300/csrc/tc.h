@@ -35,6 +35,9 @@ struct TcArgs {
   int ldy;
   float* partials;                // [t][pM][rows]
   int pM;
+  // TC_ROWPAR_CHAIN, nullable: per (token, 32-row group) sums of squares of the stored bf16 y,
+  // [M][rows / 32] (the next RMSNorm's input, folded into the next GEMM as per-token factors)
+  float* norm_ss;
   // stream-K (decode token tiles): pieces of items cut across CTAs are summed in k order by
   // the CTA that finishes an item last
   int streamk;

@@ -6,9 +6,9 @@ baseline leg may import this module.  The product path never routes through it.
 What it computes, in float64, following the pages:
   * Megatron MLP, "Tensor Parallelism (Megatron-Style)" (arunshar.com, ch. 12,
     Y = GeLU(XA)B with A split by columns, B split by rows, Z = sum_k Z_k),
-    in Llama's SwiGLU form ("Llama's version adds a second input matrix, split
-    the same way", vidyal.ai model-parallelism, "Step 1: tensor parallelism
-    slices every layer"):  y = x + (silu(x Wg) * (x Wu)) Wd.
+    in Llama's SwiGLU form (one more input matrix, split like the first,
+    vidyal.ai model-parallelism, "Step 1: tensor parallelism slices every
+    layer"):  y = x + (silu(x Wg) * (x Wu)) Wd.
   * The attention sub-block of "The Tensor-Parallel Shard Group"
     (scalablesystem.dev): QKV column-parallel, local attention over each
     shard's heads, o_proj row-parallel with one sum.

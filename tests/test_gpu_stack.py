@@ -11,21 +11,40 @@ import torch
 
 from megatron_tensor_transformer_gb300 import inputs, tpx
 from oracle import tp_oracle as O
-from tests.test_gpu_parity import REL_F, bits, check_close
+from tests.test_gpu_parity import REL_F, bits, check_close, check_h
 
 pytestmark = pytest.mark.gpu
 
 
-def check_layer(y, y_ref, what):
-    """Bar for a whole layer (two blocks composed).  The attention block's output h1 is rounded
-    to bf16 and then passes through the MLP block, whose gain carries that error on: a layer
-    gets the sum of two blocks' relF bars (1e-2).  Per element, y = h1 + MLP(b) holds up to two
-    bf16 roundings of values the size of |y| on top of that: |err| <= 2^-7 |y_ref| + 2e-2 RMS."""
-    yf, yr = O.as_f64(y), O.as_f64(y_ref)
+def check_layer(y, y_ref, h1_ref, what):
+    """A whole layer against the oracle layer whose attention output h1 is rounded to bf16 as
+    the GPU stores it (both start from the same bf16 input): relF <= 5e-3, the block bar.  Per
+    element the layer composes two blocks: y = h1 + MLP(norm(h1)) carries the attention block's
+    own error in h1 (its bf16 roundings of qkv, o_in and h1, within 2e-2 RMS(h1) per element)
+    through the residual, on top of the MLP block's (within 2e-2 RMS(y)).  So the whole layer is
+    held to the sum of the two block bars, |err| <= 2e-2 (RMS(y_ref) + RMS(h1_ref)); each block
+    is held to its own 2e-2 RMS on its own input in Layer.check_outputs."""
+    yf, yr, hr = O.as_f64(y), O.as_f64(y_ref), O.as_f64(h1_ref)
     r = O.rel_frobenius(yf, yr)
-    rms = np.sqrt(np.mean(yr * yr))
-    excess = np.abs(yf - yr) - (2.0 ** -7 * np.abs(yr) + 2e-2 * rms)
-    assert r <= 2 * REL_F and np.all(excess <= 0), f"{what}: relF {r:.3e}, worst excess {excess.max():.3e}"
+    bar = 2e-2 * (np.sqrt(np.mean(yr * yr)) + np.sqrt(np.mean(hr * hr)))
+    worst = np.abs(yf - yr).max()
+    assert r <= REL_F and worst <= bar, f"{what}: relF {r:.3e} (bar {REL_F}), max |err| {worst:.3e} (bar {bar:.3e})"
+
+
+def _align(n):
+    return (n + 255) // 256 * 256
+
+
+def layer_scratch(scratch, M, d, Q, ffn):
+    """The activations tp_layer_forward leaves in its scratch, at the offsets its declaration
+    gives: h1 [M, d], the attention output o_in [M, d], qkv [M, Q] (shard-major) and h [M, ffn]."""
+    b = _align(M * d * 2)
+    view = lambda off, n, shape: scratch[off:off + n * 2].view(torch.bfloat16).view(shape)
+    h1 = view(b, M * d, (M, d))
+    oi = view(2 * b, M * d, (M, d))
+    qk = view(4 * b, M * Q, (M, Q))
+    h = view(4 * b + _align(M * Q * 2), M * ffn, (M, ffn))
+    return h1, oi, qk, h
 
 
 @pytest.fixture(scope="module")
@@ -57,10 +76,33 @@ class Layer:
         assert tpx.tp_sync(timeout_ms=30000) == tpx.TP_OK
         return y
 
-    def oracle(self, xb):
-        y, _ = O.layer(xb, bits(self.wqkv), bits(self.wo), bits(self.wg), bits(self.wu), bits(self.wd),
-                       *self.heads)
-        return y
+    def weights(self):
+        return [bits(w) for w in (self.wqkv, self.wo, self.wg, self.wu, self.wd)]
+
+    def oracle(self, xb, weights=None):
+        """(y, h1) of the oracle layer, h1 rounded to bf16 between the blocks."""
+        return O.layer(xb, *(weights or self.weights()), *self.heads, bf16_between_blocks=True)
+
+    def check_outputs(self, xb, y, scratch, what, weights=None, rows=None):
+        """Every output of one folded-norm layer: qkv and h1 against the oracle attention block
+        on the layer's input; h and y against the oracle MLP block on the GPU's own h1 (teacher
+        forcing at the block boundary); y against the whole oracle layer.  rows: check only
+        these token rows (each output row depends on its own input row alone)."""
+        wqkv, wo, wg, wu, wd = weights or self.weights()
+        n_q, n_kv, hd = self.heads
+        M, d = xb.shape
+        Q, ffn, t = (n_q + 2 * n_kv) * hd, wg.shape[1], self.sh.t
+        sel = slice(None) if rows is None else rows
+        h1, oi, qk, h = (bits(v)[sel] for v in layer_scratch(scratch, M, d, Q, ffn))
+        xb, yb = xb[sel], bits(y)[sel]
+        h1_ref, qkv_ref = O.proj(O.rmsnorm(xb), wqkv, wo, n_q, n_kv, hd, residual=xb)
+        cols = np.concatenate([O.colpar_columns("qkv", s, t, n_q=n_q, n_kv=n_kv, hd=hd)[0] for s in range(t)])
+        check_close(O.as_f64(qk), qkv_ref[:, cols], what=f"{what}: qkv")
+        check_close(O.as_f64(h1), h1_ref, what=f"{what}: h1 (attention block)")
+        y_tf, h_ref = O.mlp(O.rmsnorm(h1), wg, wu, wd, residual=h1)
+        check_h(h, h_ref, what=f"{what}: h")
+        check_close(O.as_f64(yb), y_tf, what=f"{what}: y (MLP block on the layer's own h1)")
+        check_layer(yb, *self.oracle(xb, weights), what=f"{what}: y (whole layer)")
 
     def check_blocks(self, xb, scratch_dev, ws, what):
         """Each block on its own, both fed from the oracle chain (its bf16 input x, and its
@@ -103,26 +145,31 @@ def test_layer_stack_per_layer_and_drift(dev):
     xg = x0                            # GPU chain
     for L, lay in enumerate(layers):
         lay.check_blocks(xo, scratch, ws, what=f"layer {L}")
-        y_ref = lay.oracle(xo)
+        y_ref, _ = lay.oracle(xo)
         y = lay.gpu(torch.from_numpy(xo.view(np.int16).copy()).view(torch.bfloat16).to(dev), scratch, ws)
-        check_layer(bits(y), y_ref, what=f"layer {L} on the oracle chain's input")
+        lay.check_outputs(xo, y, scratch, what=f"layer {L} on the oracle chain's input")
         xg = lay.gpu(xg, scratch, ws)
         xo = O.f64_to_bf16_bits(y_ref)
     drift = O.rel_frobenius(bits(xg), O.as_f64(xo))
     assert drift <= 2e-2, f"end-to-end drift over {nl} layers: relF {drift:.3e}"
 
 
-def test_405b_layer_full_size_sampled_tokens(dev):
-    """One full 405B-shaped layer (d 16384, ffn 53248, 128 q / 8 kv heads, t=8) on two
-    decode tokens, every output against the oracle."""
+def test_405b_layer_full_size_decode_batch(dev):
+    """One full 405B-shaped layer (d 16384, ffn 53248, 128 q / 8 kv heads, t=8) at the
+    pipeline-stage stack's decode batch, M=16, through the default tp_layer_forward (the two
+    folded-norm launches the stack runs): every output against the oracle, then each block on
+    its own through the split path."""
     lay = Layer(16384, 53248, 128, 8, 128, 8, 0, dev, seed=0)
-    M = 2
+    M = 16
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, 16384), 1.0, 0, inputs.STREAM_X, dev)
-    lay.check_blocks(bits(x), scratch, ws, what="405B layer, 2 tokens")
+    n0 = tpx.tp_launch_count()
     y = lay.gpu(x, scratch, ws)
-    check_layer(bits(y), lay.oracle(bits(x)), what="405B layer, 2 tokens")
+    assert tpx.tp_launch_count() - n0 == 2
+    w = lay.weights()
+    lay.check_outputs(bits(x), y, scratch, what="405B layer, 16 tokens", weights=w)
+    lay.check_blocks(bits(x), scratch, ws, what="405B layer, 16 tokens")
 
 
 @pytest.mark.parametrize("M,wtype,fl", [(16, tpx.TP_BF16, 0), (5, tpx.TP_BF16, 0),
@@ -133,9 +180,8 @@ def test_405b_layer_full_size_sampled_tokens(dev):
 def test_layer_norm_folded_into_blocks(dev, M, wtype, fl):
     """Decode layers run as two launches: the RMSNorms become per-token factors on the
     column-parallel accumulators (the attention block computes its input's factors, and its
-    fold those of h1).  Against the oracle, against the path with separate RMSNorm launches
-    (no bf16 rounding of the normalised input here, so the two differ by rounding only), and
-    bit for bit from run to run."""
+    fold those of h1).  Every output against the oracle (e4m3 weights: on the dequantised
+    weights), the path with separate RMSNorm launches as well, and bit for bit from run to run."""
     # e4m3 weights stream in 128-wide k-blocks: the down projection's K per shard (ffn / t) must
     # be a multiple of 128 for the one-launch block
     d, ffn, n_q, n_kv, hd, t = 2048, 6656 if wtype == tpx.TP_BF16 else 7168, 16, 8, 128, 8
@@ -158,15 +204,72 @@ def test_layer_norm_folded_into_blocks(dev, M, wtype, fl):
                          scratch, ws, flags=tpx.TP_F_SPLIT_BLOCK)
     assert tpx.tp_sync(timeout_ms=30000) == tpx.TP_OK
     if wtype == tpx.TP_BF16:
-        check_layer(bits(y), lay.oracle(bits(x)), what=f"folded-norm layer M={M}")
+        w = lay.weights()
     else:
-        deq = []
-        for w in (lay.wqkv, lay.wo, lay.wg, lay.wu, lay.wd):
-            q, s = O.quantize_fp8_per_channel(O.as_f64(bits(w)))
-            deq.append(O.dequantize_fp8(q, s))
-        y_ref, _ = O.layer(bits(x), *deq, n_q, n_kv, hd)
-        check_layer(bits(y), y_ref, what=f"folded-norm fp8 layer M={M}")
-    check_layer(bits(y), O.as_f64(bits(y_split)), what="folded vs separate norms")
+        w = []
+        for m in (lay.wqkv, lay.wo, lay.wg, lay.wu, lay.wd):
+            q, sc = O.quantize_fp8_per_channel(O.as_f64(bits(m)))
+            w.append(O.dequantize_fp8(q, sc))
+    y_split_ref, h1_ref = O.layer(bits(x), *w, n_q, n_kv, hd, bf16_between_blocks=True)
+    check_layer(bits(y_split), y_split_ref, h1_ref, what=f"separate-norm layer M={M}")
+    y = lay.gpu(x, scratch, ws, fl)         # the scratch again holds the folded path's activations
+    lay.check_outputs(bits(x), y, scratch, what=f"folded-norm layer M={M}", weights=w)
     for _ in range(2):
         y2 = lay.gpu(x, scratch, ws, fl)
         assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def _fp8_layer(lay, d, ffn, n_q, n_kv, hd, t):
+    lay.sh = tpx.make_shape(d, ffn=ffn, n_q=n_q, n_kv=n_kv, hd=hd, t=t, wtype=tpx.TP_FP8_E4M3)
+    lay.q_w, lay.q = tpx.tp_partition_weights(lay.sh, tpx.TP_W_QKV, lay.wqkv)
+    lay.o_w, lay.o = tpx.tp_partition_weights(lay.sh, tpx.TP_W_O, lay.wo)
+    lay.gu_w, lay.gu = tpx.tp_partition_weights(lay.sh, tpx.TP_W_GATE_UP, lay.wg, lay.wu)
+    lay.dn_w, lay.dn = tpx.tp_partition_weights(lay.sh, tpx.TP_W_DOWN, lay.wd)
+    w = []
+    for m in (lay.wqkv, lay.wo, lay.wg, lay.wu, lay.wd):
+        q, sc = O.quantize_fp8_per_channel(O.as_f64(bits(m)))
+        w.append(O.dequantize_fp8(q, sc))
+    return w
+
+
+@pytest.mark.parametrize("M,t,wtype", [(200, 8, tpx.TP_BF16), (65, 2, tpx.TP_BF16), (300, 8, tpx.TP_FP8_E4M3)],
+                         ids=["bf16-200", "bf16-65-t2", "fp8-300"])
+def test_layer_prefill_norm_folded(dev, M, t, wtype):
+    """Prefill layers (M > 64): the RMSNorms become per-token factors on the tcgen05 GEMMs'
+    accumulators (the factors of x from one pass over x, those of h1 from the sums of squares
+    the o_proj epilogue leaves while it writes h1), so the normalised activations are never
+    written.  Every output against the oracle, the separate-norm path too, and bit for bit from
+    run to run."""
+    d, ffn, n_q, n_kv, hd = 2048, 6656 if wtype == tpx.TP_BF16 else 7168, 16, 8, 128
+    lay = Layer(d, ffn, n_q, n_kv, hd, t, 0, dev, seed=5)
+    w = lay.weights() if wtype == tpx.TP_BF16 else _fp8_layer(lay, d, ffn, n_q, n_kv, hd, t)
+    scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
+    ws = tpx.new_workspace(lay.sh, M, dev)
+    x = inputs.normal_bf16((M, d), 1.0, 5, inputs.STREAM_X, dev)
+    y_split = lay.gpu(x, scratch, ws, tpx.TP_F_SPLIT_BLOCK)
+    y_split_ref, h1_ref = O.layer(bits(x), *w, n_q, n_kv, hd, bf16_between_blocks=True)
+    check_layer(bits(y_split), y_split_ref, h1_ref, what=f"separate-norm prefill layer M={M}")
+    n0 = tpx.tp_launch_count()
+    y = lay.gpu(x, scratch, ws)
+    # factors of x, QKV, attention stand-in, o_proj, factors of h1, gate/up, down
+    # (e4m3 weights: each GEMM's weights widened first)
+    assert tpx.tp_launch_count() - n0 == (7 if wtype == tpx.TP_BF16 else 11)
+    lay.check_outputs(bits(x), y, scratch, what=f"folded-norm prefill layer M={M} t={t}", weights=w)
+    y2 = lay.gpu(x, scratch, ws)
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
+def test_70b_layer_prefill_norm_folded_sampled_rows(dev):
+    """A 70B-shaped pre-norm layer (d 8192, ffn 28672, 64 q / 8 kv heads, t = 8) at prefill,
+    M = 1000, through tp_layer_forward: every output on sampled token rows (first, last, tile
+    edges) against the oracle."""
+    lay = Layer(8192, 28672, 64, 8, 128, 8, 0, dev, seed=6)
+    M = 1000
+    scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
+    ws = tpx.new_workspace(lay.sh, M, dev)
+    x = inputs.normal_bf16((M, 8192), 1.0, 6, inputs.STREAM_X, dev)
+    y = lay.gpu(x, scratch, ws)
+    rows = np.array([0, 1, 127, 128, 255, 256, 511, 512, 767, 768, 998, 999])
+    w = [O.as_f64(b) for b in lay.weights()]
+    lay.check_outputs(bits(x), y, scratch, what="70B prefill layer, sampled rows", weights=w, rows=rows)
+    assert not torch.isnan(y).any()
