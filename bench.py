@@ -21,7 +21,7 @@ streams more than the 129 MB L2 per step, so no flush is needed between steps.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tpx|reference] [--workload NAME]
 
 --workload runs one configuration (or one of the extra ones: 70b-fp8x-*, 405b-layer-decode,
-70b-lm-head-decode, 70b-attn-decode) and prints its record as the line.  --impl reference times
+70b-prenorm-prefill, 70b-lm-head-decode, 70b-attn-decode) and prints its record as the line.  --impl reference times
 the float64 CPU oracle on a bounded sample of the headline workload (there is no reference GPU
 implementation to run).
 """
@@ -53,7 +53,10 @@ LAYERS = {
     "70b-fp8x-prefill": (8192, 28672, 64, 8, 128, 8, 8192, 2, 1),
     "405b-layer-decode": (16384, 53248, 128, 8, 128, 8, 16, 0, 1),
     "405b-stack-decode": (16384, 53248, 128, 8, 128, 8, 16, 0, 10),
+    "70b-prenorm-prefill": (8192, 28672, 64, 8, 128, 8, 4096, 0, 1),
 }
+# run through tp_layer_forward (pre-norm layers: RMSNorm + residual around both blocks)
+PRENORM = {"405b-stack-decode", "70b-prenorm-prefill"}
 MLP8B = (4096, 14336, 8, (1, 8, 32, 64))
 EXTRA = ["70b-lm-head-decode", "70b-attn-decode"]
 
@@ -404,7 +407,7 @@ def run_layer(hx, name, K, W, kernel_flags=0, t_override=0):
     h = torch.empty((M, ffn), dtype=torch.bfloat16, device=hx.dev)
     ws = tpx.new_workspace(sh, M, hx.dev, flags=kf)
     s = hx.stream
-    if nl > 1:
+    if name in PRENORM:
         scratch = torch.empty(tpx.tp_layer_scratch_bytes(sh, M), dtype=torch.uint8, device=hx.dev)
         xa, xb = torch.empty_like(x), torch.empty_like(x)
 
