@@ -681,7 +681,7 @@ def run_reference(args, rank, world):
 
 
 KERNEL_FLAGS = {"auto": 0, "tc": "TP_F_KERNEL_TC", "skinny": "TP_F_KERNEL_SKINNY", "split": "TP_F_SPLIT_BLOCK",
-                "hilo": "TP_F_FP8_HILO"}
+                "hilo": "TP_F_FP8_HILO", "foldnorm": "TP_F_FOLD_NORM"}
 
 
 def run_one(hx, name, K, W, args):
@@ -712,7 +712,8 @@ def main():
     ap.add_argument("--t", type=int, default=0, help="shard count for the layer workloads (default: 8)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_FLAGS),
                     help="force the tcgen05 or the mma.sync decode kernels, or separate launches for the "
-                         "two halves of a block (default: library policy, one fused launch per block)")
+                         "two halves of a block, or (foldnorm) prefill layers with their RMSNorms folded into "
+                         "the GEMMs (default: library policy, one fused launch per decode block)")
     ap.add_argument("--cpu-sample", default=None, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.cpu_sample:                     # child process of cpu_baseline

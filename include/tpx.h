@@ -145,6 +145,14 @@ typedef struct {
                                      approximates the bf16-activation product (fp32 sums, in another
                                      order) rather than equalling it.  No effect on bf16 weights or where
                                      the one-launch block does not apply */
+#define TP_F_FOLD_NORM 0x800u     /* tp_layer_forward at prefill token counts (M > 64, every GEMM on the
+                                     tcgen05 path): fold both RMSNorms into the GEMMs as per-token factors
+                                     on the column-parallel accumulators (x's factors from one pass over x,
+                                     h1's from sums of squares the o_proj epilogue leaves), so the
+                                     normalised activations are never written.  Opt-in: measured on the
+                                     70B layer at M = 4096 it is slower (4.79 ms against 4.66 ms), the
+                                     epilogue work costing more than the norm passes it saves.  Decode
+                                     layers always fold the norms into their two block launches */
 #define TP_F_SPLIT_BLOCK 0x80u    /* tp_mlp_forward / tp_proj_forward: run the two halves as separate
                                      launches.  By default a decode block (M <= 64, 128-row tiles; k %
                                      64 for bf16 weights, k % 128 for e4m3, see TP_F_FP8_HILO) runs as
@@ -210,7 +218,8 @@ tp_status tp_proj_forward(const tp_packed_desc* qkv /* host */, const void* qkv_
  * 3B, qkv [M, (n_q+2n_kv)hd] (shard-major) at 4B and h [M, ffn] at 4B + round_up(M*Q*2, 256);
  * after the call h1, the attention output, qkv and h hold this layer's values.  At decode token
  * counts the norms are folded into the two block launches (per-token factors on the
- * column-parallel accumulators) and a, b are not written. */
+ * column-parallel accumulators) and a, b are not written; at prefill the same with
+ * TP_F_FOLD_NORM. */
 size_t tp_layer_scratch_bytes(const tp_shape* shape /* host */, int32_t M);
 tp_status tp_layer_forward(const tp_packed_desc* qkv /* host */, const void* qkv_w,
                            const tp_packed_desc* o /* host */, const void* o_w,

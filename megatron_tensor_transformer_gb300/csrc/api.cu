@@ -276,8 +276,8 @@ using bf16 = __nv_bfloat16;
 // threshold, the mma.sync skinny kernel otherwise; flags can force either one.
 constexpr int kTcMinM = 0;  // tcgen05 wherever the geometry allows: with PDL it wins the whole step
 constexpr uint32_t kKernelFlags = TP_F_KERNEL_SKINNY | TP_F_KERNEL_TC;
-constexpr uint32_t kFwdFlags =
-    TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT | TP_F_FP8_HILO;
+constexpr uint32_t kFwdFlags = TP_F_UNFUSED_REDUCE | kKernelFlags | TP_F_SERIAL | TP_F_SPLIT_BLOCK | TP_F_FP8_ACT |
+                               TP_F_FP8_HILO | TP_F_FOLD_NORM;
 
 bool pick_tc(uint32_t flags, int rows, int K, bool fp8, int M) {
   if (flags & TP_F_KERNEL_SKINNY) return false;
@@ -664,11 +664,12 @@ bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {
   return a.n_q_heads == b.n_q_heads && a.n_kv_heads == b.n_kv_heads && a.head_dim == b.head_dim;
 }
 
-// A prefill layer whose four GEMMs all run on the tcgen05 path, with the chained row-parallel
-// fold (no flag asking for anything else): the RMSNorms fold into their epilogues.
+// A prefill layer asked to fold its norms (TP_F_FOLD_NORM) whose four GEMMs all run on the tcgen05
+// path, with the chained row-parallel fold: the RMSNorms fold into their epilogues.
 bool prefill_fold(uint32_t flags, const tp_packed_desc* q, const tp_packed_desc* o, const tp_packed_desc* gu,
                   const tp_packed_desc* dn, int M) {
-  if (M <= kFusedMaxM || (flags & (TP_F_FP8_ACT | TP_F_SPLIT_BLOCK | TP_F_KERNEL_SKINNY | TP_F_UNFUSED_REDUCE)))
+  if (!(flags & TP_F_FOLD_NORM) || M <= kFusedMaxM ||
+      (flags & (TP_F_FP8_ACT | TP_F_SPLIT_BLOCK | TP_F_KERNEL_SKINNY | TP_F_UNFUSED_REDUCE)))
     return false;
   if (q->shape.d % 32 != 0) return false;
   for (const tp_packed_desc* d : {q, o, gu, dn})

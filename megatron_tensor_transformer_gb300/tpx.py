@@ -20,6 +20,7 @@ TP_F_UNFUSED_REDUCE, TP_F_FP32_COLPAR_OUT = 0x1, 0x2
 TP_F_KERNEL_SKINNY, TP_F_KERNEL_TC, TP_F_SERIAL, TP_F_SPLIT_BLOCK = 0x10, 0x20, 0x40, 0x80
 TP_F_FP8_ACT = 0x200
 TP_F_FP8_HILO = 0x400
+TP_F_FOLD_NORM = 0x800
 
 EXPORTS = ["tp_packed_bytes", "tp_describe", "tp_partition_weights", "tp_workspace_bytes",
            "tp_mlp_forward", "tp_proj_forward", "tp_reduce_partials", "tp_colpar_forward",

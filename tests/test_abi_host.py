@@ -116,7 +116,7 @@ def test_argument_errors_before_launch():
     gu, dn = tpx.tp_describe(sh, tpx.TP_W_GATE_UP), tpx.tp_describe(sh, tpx.TP_W_DOWN)
     assert _call_mlp(gu, dn, M=-1) == tpx.TP_ERR_INVALID_ARG
     assert _call_mlp(gu, dn, flags=0x100) == tpx.TP_ERR_INVALID_ARG              # unknown flag bit
-    assert _call_mlp(gu, dn, flags=0x800) == tpx.TP_ERR_INVALID_ARG
+    assert _call_mlp(gu, dn, flags=0x1000) == tpx.TP_ERR_INVALID_ARG
     # the hi/lo e4m3 block flag is a block flag: accepted (the call goes on to the workspace
     # check), alone or with the widening flag
     for fl in (tpx.TP_F_FP8_HILO, tpx.TP_F_FP8_HILO | tpx.TP_F_KERNEL_TC):

@@ -235,40 +235,41 @@ def _fp8_layer(lay, d, ffn, n_q, n_kv, hd, t):
 @pytest.mark.parametrize("M,t,wtype", [(200, 8, tpx.TP_BF16), (65, 2, tpx.TP_BF16), (300, 8, tpx.TP_FP8_E4M3)],
                          ids=["bf16-200", "bf16-65-t2", "fp8-300"])
 def test_layer_prefill_norm_folded(dev, M, t, wtype):
-    """Prefill layers (M > 64): the RMSNorms become per-token factors on the tcgen05 GEMMs'
-    accumulators (the factors of x from one pass over x, those of h1 from the sums of squares
-    the o_proj epilogue leaves while it writes h1), so the normalised activations are never
-    written.  Every output against the oracle, the separate-norm path too, and bit for bit from
-    run to run."""
+    """Prefill layers (M > 64), with separate RMSNorm launches (the default) and with
+    TP_F_FOLD_NORM, where the norms become per-token factors on the tcgen05 GEMMs' accumulators
+    (the factors of x from one pass over x, those of h1 from the sums of squares the o_proj
+    epilogue leaves while it writes h1) and the normalised activations are never written.
+    Every output of both against the oracle, and bit for bit from run to run."""
     d, ffn, n_q, n_kv, hd = 2048, 6656 if wtype == tpx.TP_BF16 else 7168, 16, 8, 128
     lay = Layer(d, ffn, n_q, n_kv, hd, t, 0, dev, seed=5)
     w = lay.weights() if wtype == tpx.TP_BF16 else _fp8_layer(lay, d, ffn, n_q, n_kv, hd, t)
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, d), 1.0, 5, inputs.STREAM_X, dev)
-    y_split = lay.gpu(x, scratch, ws, tpx.TP_F_SPLIT_BLOCK)
+    y_split = lay.gpu(x, scratch, ws)
     y_split_ref, h1_ref = O.layer(bits(x), *w, n_q, n_kv, hd, bf16_between_blocks=True)
     check_layer(bits(y_split), y_split_ref, h1_ref, what=f"separate-norm prefill layer M={M}")
+    fold = tpx.TP_F_FOLD_NORM
     n0 = tpx.tp_launch_count()
-    y = lay.gpu(x, scratch, ws)
+    y = lay.gpu(x, scratch, ws, fold)
     # factors of x, QKV, attention stand-in, o_proj, factors of h1, gate/up, down
     # (e4m3 weights: each GEMM's weights widened first)
     assert tpx.tp_launch_count() - n0 == (7 if wtype == tpx.TP_BF16 else 11)
     lay.check_outputs(bits(x), y, scratch, what=f"folded-norm prefill layer M={M} t={t}", weights=w)
-    y2 = lay.gpu(x, scratch, ws)
+    y2 = lay.gpu(x, scratch, ws, fold)
     assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
 
 
 def test_70b_layer_prefill_norm_folded_sampled_rows(dev):
     """A 70B-shaped pre-norm layer (d 8192, ffn 28672, 64 q / 8 kv heads, t = 8) at prefill,
-    M = 1000, through tp_layer_forward: every output on sampled token rows (first, last, tile
-    edges) against the oracle."""
+    M = 1000, through tp_layer_forward with the norms folded (TP_F_FOLD_NORM): every output on
+    sampled token rows (first, last, tile edges) against the oracle."""
     lay = Layer(8192, 28672, 64, 8, 128, 8, 0, dev, seed=6)
     M = 1000
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, 8192), 1.0, 6, inputs.STREAM_X, dev)
-    y = lay.gpu(x, scratch, ws)
+    y = lay.gpu(x, scratch, ws, tpx.TP_F_FOLD_NORM)
     rows = np.array([0, 1, 127, 128, 255, 256, 511, 512, 767, 768, 998, 999])
     w = [O.as_f64(b) for b in lay.weights()]
     lay.check_outputs(bits(x), y, scratch, what="70B prefill layer, sampled rows", weights=w, rows=rows)
