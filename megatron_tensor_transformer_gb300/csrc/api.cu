@@ -655,7 +655,11 @@ tp_status run_fused(int kind, const tp_packed_desc* d1, const void* w1, const tp
   a.eps = eps;
   a.err = tc_error_word();
   if (!a.err) return TP_ERR_CUDA;
-  return launch_fused(a, st, (flags & TP_F_SERIAL) == 0) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
+  const bool pdl = (flags & TP_F_SERIAL) == 0;
+  // split activations: the input's per-token maxima, computed just before the block
+  if (a.split && launch_token_absmax(x, M, a.d, fused_xmax_words(a.sync, a.d), pdl, st) != cudaSuccess)
+    return TP_ERR_CUDA;
+  return launch_fused(a, st, pdl) == cudaSuccess ? TP_OK : TP_ERR_CUDA;
 }
 
 bool same_block(const tp_shape& a, const tp_shape& b, bool mlp) {

@@ -40,7 +40,7 @@ namespace {
 constexpr int FBM = 128, FBK = 64, kRing = 8;
 constexpr int kProducer = 4, kMma = 5;
 // sync words (all zero between launches)
-constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncXS = 4, kSyncDone = 8,
+constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncDone = 8,
               kSyncTicket = 128;
 
 // bf16 weights: each stage holds one 64-wide k-block, the 128 x 64 bf16 weight tile (128-byte
@@ -177,28 +177,10 @@ __device__ __forceinline__ void split_pair(uint32_t xb, float inv, uint16_t& hi,
 }
 // the per-(shard, token) maxima of |stage-2 input| and the per-token maxima of |x| (float bits)
 __device__ __forceinline__ unsigned* hmax_of(const FusedArgs& a) { return a.sync + fused_hmax_off(a.d); }
-__device__ __forceinline__ unsigned* xmax_of(const FusedArgs& a) {
-  return a.sync + fused_hmax_off(a.d) + 8 * kFusedMaxMWords;
-}
+__device__ __forceinline__ unsigned* xmax_of(const FusedArgs& a) { return fused_xmax_words(a.sync, a.d); }
 // the split scale 2^e of a token from its maximum's bits
 __device__ __forceinline__ int split_exp_bits(const unsigned* p) { return split_exp(__uint_as_float(__ldcg(p))); }
 __device__ __forceinline__ void conv_bar() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-// Bounded wait (~2 s) until every CTA has added its share of the maxima of |x|.
-__device__ bool wait_xmax(const FusedArgs& a, volatile int* abort_flag) {
-  const unsigned* cnt = a.sync + kSyncXS;
-  if (ld_acquire(cnt) < gridDim.x) {
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t i = 1; ld_acquire(cnt) < gridDim.x; ++i) {
-      if (*abort_flag) return false;
-      if ((i & 63u) == 0 && globaltimer_ns() - t0 > 2000000000ull) {
-        raise(a.err, 44, abort_flag);
-        return false;
-      }
-      __nanosleep(64);
-    }
-  }
-  return true;
-}
 // The largest |value| a warp's lanes hold for each of 16 tokens, into the shard's maxima
 // (non-negative floats order like their bits).
 __device__ __forceinline__ void warp_token_max(const FusedArgs& a, int s, int mf, float (&mv)[16]) {
@@ -694,32 +676,11 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
     }
   } else if (warp >= 6) {
     if constexpr (SPLIT) {
-      // Split converters.  First the per-token maxima of |x|: each CTA reduces a slice of the
-      // columns of every token, adds it (atomic max) to the grid's maxima and counts itself in.
-      __shared__ unsigned s_xmax[kFusedMaxM];
-      const int cw = warp - 6, ct = 32 * cw + lane;
+      // Split converters.  The per-token maxima of |x| were written by the kernel launched just
+      // before this one (launch_token_absmax), complete once the grids this one depends on are.
+      const int cw = warp - 6;
       griddep_wait();
-      if (ct < kFusedMaxM) s_xmax[ct] = 0u;
-      conv_bar();
-      {
-        const int nch = a.d / 8;  // 16-byte chunks of a row
-        const int c_lo = (int)((long long)nch * blockIdx.x / gridDim.x);
-        const int cnt = (int)((long long)nch * (blockIdx.x + 1) / gridDim.x) - c_lo;
-        for (int i = ct; i < a.M * cnt; i += 32 * C::kConvWarps) {
-          const int m = i / cnt, c = c_lo + i % cnt;
-          const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.d + 8 * c);
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-          float mx = 0.f;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(u[j])), fabsf(bf16_hi(u[j]))));
-          if (mx > 0.f) atomicMax(s_xmax + m, __float_as_uint(mx));
-        }
-      }
-      conv_bar();
-      if (ct < a.M && s_xmax[ct] != 0u) atomicMax(xmax_of(a) + ct, s_xmax[ct]);
-      conv_bar();  // then one release by thread 0 covers the group's atomics (barrier, then release)
-      if (ct == 0) red_release_add(a.sync + kSyncXS, 1u);
-      bool ok = wait_xmax(a, abort_flag);
+      bool ok = true;
       // each warp splits BN/4 tokens, 8 lanes a token, lane l the 16-wide k chunk l % 8
       constexpr int NIT = BN / 16;
       const int c = lane & 7;
@@ -880,7 +841,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       epi_bar();
       if (threadIdx.x == 0) red_release_add(a.sync + kSyncInNorm, 1u);
     }
-    bool scale_ready = a.in_norm == 0, xmax_ready = false;
+    bool scale_ready = a.in_norm == 0;
     int q = 0, it = 0;
     while (true) {
       const int rr = q % kRing;
@@ -903,11 +864,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       float tsc0[16];
       if constexpr (SPLIT) {
         if (f.stage == 1) {
-          if (!xmax_ready) {
-            if (!__all_sync(0xffffffffu, wait_xmax(a, abort_flag))) break;
-            xmax_ready = true;
-          }
-          split_max = xmax_of(a);
+          split_max = xmax_of(a);  // written before this launch (the epilogue has passed griddep_wait)
         } else {
           if (!__all_sync(0xffffffffu, wait_stage1(a, f.s, abort_flag))) break;
           split_max = hmax_of(a) + f.s * kFusedMaxMWords;
@@ -1043,8 +1000,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       a.sync[kSyncInNorm] = 0u;
       for (int s = 0; s < 8; ++s) a.sync[kSyncDone + s] = 0u;
       if (SPLIT) {
-        a.sync[kSyncXS] = 0u;
-        for (int i = 0; i < 9 * kFusedMaxMWords; ++i) hmax_of(a)[i] = 0u;  // h maxima, then x maxima
+        for (int i = 0; i < 8 * kFusedMaxMWords; ++i) hmax_of(a)[i] = 0u;  // the h (or o_in) maxima
       }
       if (*reinterpret_cast<volatile unsigned*>(a.err) != 0u) {
         for (int rt = 0; rt < a.d / FBM; ++rt) a.sync[kSyncTicket + rt] = 0u;

@@ -56,8 +56,13 @@ constexpr int kFusedMaxMWords = 64;  // per-token arrays are sized for kFusedMax
 inline int fused_norm_words(int d) { return kFusedMaxMWords * (d / 128) + 2 * kFusedMaxMWords; }
 // Sync area words: 128 + one ticket per 128-row output tile, then (split activations) the
 // per-(shard, token) maxima of the stage-2 input [8][64] (zero between launches) and the
-// input's per-token scales [64].
+// input's per-token maxima [64] (written before each launch).
 __host__ __device__ inline int fused_hmax_off(int d) { return (128 + d / 128 + 31) / 32 * 32; }
+// the input's per-token maxima of |x| (float bits), written before each split-activation block by
+// launch_token_absmax
+__host__ __device__ inline unsigned* fused_xmax_words(unsigned* sync, int d) {
+  return sync + fused_hmax_off(d) + 8 * kFusedMaxMWords;
+}
 inline int fused_sync_words(int d) { return fused_hmax_off(d) + 8 * kFusedMaxMWords + kFusedMaxMWords; }
 
 // Whether the fused kernel supports this block (128-row tiles, M <= 64; 64-wide k-blocks for bf16

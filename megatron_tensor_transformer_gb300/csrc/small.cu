@@ -161,6 +161,52 @@ cudaError_t launch_rms_factors_from_ss(const float* ss, float eps, int M, int d,
   return cudaGetLastError();
 }
 
+// Per-token max |x| for the hi/lo split of an e4m3 decode block (exact: a maximum does not round),
+// one block per token: eight values per thread per step, a shuffle tree per warp, then the warps.
+// As a programmatic dependent it first lets the block kernel after it launch (that kernel starts
+// streaming weights and waits for this one before it reads the maxima), then waits for the kernel
+// before it, which may have written x.
+__global__ void token_absmax_kernel(const __nv_bfloat16* __restrict__ x, int d, unsigned* __restrict__ out) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ float part[32];
+  const int m = blockIdx.x;
+  const __nv_bfloat16* xr = x + (size_t)m * d;
+  float mx = 0.f;
+  for (int i = threadIdx.x * 8; i < d; i += blockDim.x * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(xr + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = mx;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) out[m] = __float_as_uint(v);
+  }
+}
+
+cudaError_t launch_token_absmax(const __nv_bfloat16* x, int M, int d, unsigned* out, bool pdl, cudaStream_t st) {
+  if (M <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, token_absmax_kernel, x, d, out);
+  note_launch();
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // One-token attention per shard: q head h (shard s = h / nq_s) returns the v of its kv group,
 // which lives in the same shard.  qkv is shard-major [q_s | k_s | v_s]; o_in is in head order.
 // Prefill with e4m3 weights: each shard is widened once per call, exactly, to the bf16 codes

@@ -27,6 +27,10 @@ cudaError_t launch_embed(const uint8_t* table, uint64_t stride, int vs, int t, i
 cudaError_t launch_rms_factors(const __nv_bfloat16* x, float eps, int M, int d, float* r, cudaStream_t st);
 // The same factors from per-(token, 32-row group) sums of squares ss [M][d / 32], summed in group order.
 cudaError_t launch_rms_factors_from_ss(const float* ss, float eps, int M, int d, float* r, cudaStream_t st);
+// Per-token max |x[m][k]| over k as float bits, out[m] for m < M, x [M, d] bf16 (d % 8 == 0): the split
+// scales of an e4m3 decode block's input.  pdl: launched as a programmatic dependent (it waits for the
+// kernel before it, and lets the block after it launch at once).
+cudaError_t launch_token_absmax(const __nv_bfloat16* x, int M, int d, unsigned* out, bool pdl, cudaStream_t st);
 cudaError_t launch_attn1(const __nv_bfloat16* qkv, int M, int n_q, int n_kv, int hd, int t,
                          __nv_bfloat16* o_in, cudaStream_t st);
 
