@@ -650,6 +650,16 @@ def cpu_baseline(name, seconds):
                            "sample": o["sample"]}}
 
 
+def workload_config(name):
+    """The configuration record of a workload, as the GPU arm prints it."""
+    if name == "8b-mlp-decode":
+        D, FFN, T, MS = MLP8B
+        return {"workload": name, "d": D, "ffn": FFN, "t": T, "M": list(MS), "tokens_per_step": sum(MS)}
+    d, ffn, n_q, n_kv, hd, t, M, wkind, nl = LAYERS[name]
+    return {"workload": name, "layers": nl, "d": d, "ffn": ffn, "n_q": n_q, "n_kv": n_kv, "head_dim": hd, "t": t,
+            "M": M, "weights_gb_per_step": (1.0 if wkind else 2.0) * layer_params(d, ffn, n_q, n_kv, hd) * nl / 1e9}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the float64 oracle on this host's cores, one bounded sample of the
     headline workload per step (cpu_setup), in the headline's metric and unit."""
@@ -670,7 +680,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": unit, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name},
+        "config": workload_config(name),
         "cpu_baseline": {"value": value, "unit": unit, "cores": cores(), "kind": "oracle",
                          "sample": f"each step: {what}"},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
