@@ -58,19 +58,26 @@ constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3,
 // converter warps split each activation tile, in place, into the e4m3 tiles hi and lo (rows 0..BN-1
 // and BN..2BN-1 of the same bytes); the MMA multiplies e4m3 x e4m3 with N = 2 BN, and the
 // epilogue adds the two column halves before the scales.
+// Split activations take two 128-wide k-blocks per stage (kSub): the MMA-issuing thread pays a
+// fixed cost per stage (two mbarrier waits and two commits besides the MMAs; measured alone, about
+// 270 ns for one 16 KB k-block), which capped the block at one k-block per 425 ns per SM; per
+// 32 KB stage the same cost covers twice the bytes.
 template <int BN, bool FP8, bool SPLIT = false>
 struct FCfg {
-  static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per stage
-  static constexpr int kABytes = FP8 ? FBM * kKB : FBM * kKB * 2;
+  static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per k-block
+  static constexpr int kSub = SPLIT ? 2 : 1;               // k-blocks per stage
+  static constexpr int kABytes1 = FP8 ? FBM * kKB : FBM * kKB * 2;  // one k-block of weights
+  static constexpr int kABytes = kABytes1 * kSub;
   static constexpr int kBSub = BN * FBK * 2;               // one 64-wide activation tile
-  static constexpr int kBBytes = kBSub * (kKB / FBK);
+  static constexpr int kBBytes1 = kBSub * (kKB / FBK);     // one k-block of activations
+  static constexpr int kBBytes = kBBytes1 * kSub;
   static constexpr int kStageBytes = kABytes + kBBytes;
   // activation ring (e4m3 only)
   // split: a slot is refilled only after the MMA has read it, and its tile then takes an L2 round
   // trip and the split before the MMA can use it, so the ring must cover that whole loop
-  static constexpr int kSB = SPLIT ? (kBBytes <= 4096 ? 12 : (kBBytes <= 8192 ? 8 : 6))
+  static constexpr int kSB = SPLIT ? (kBBytes <= 8192 ? 8 : (kBBytes <= 16384 ? 4 : 3))
                                    : (FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0);
-  static constexpr int kMaxStages = SPLIT ? 12 : (FP8 ? 10 : 8);
+  static constexpr int kMaxStages = SPLIT ? 6 : (FP8 ? 10 : 8);
   // split: no tensor-memory A slots to feed, so more of the 227 KB goes to weights in flight
   static constexpr int kRingBytes = (SPLIT ? 224 : 200) * 1024 - kSB * kBBytes;
   static constexpr int kUnitBytes = FP8 ? kABytes : kStageBytes;
@@ -427,8 +434,9 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         mbar_arrive(ifull0 + 8 * r);
         ++q;
       };
-      auto load_a = [&](const FItem& f, int kb, int st) {
-        const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes), bar = full0 + 8 * st;
+      // k-block kb of item f into sub-block u of stage st
+      auto load_a = [&](const FItem& f, int kb, int st, int u = 0) {
+        const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes + (size_t)u * C::kABytes1), bar = full0 + 8 * st;
         if (f.stage == 1)
           tma_load_3d_hint(dst, &tmA1, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
         else
@@ -448,29 +456,33 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       int item = blockIdx.x;
       FItem f = fdecode(a, item, C::kKB);
       if constexpr (FP8) {
-        // weights only: the activation tiles have a producer warp of their own
-        auto issue_w = [&](const FItem& g, int kb) {
+        // weights only: the activation tiles have a producer warp of their own.  Stage j of an
+        // item holds its k-blocks kSub j .. (the last stage may hold fewer)
+        auto issue_w = [&](const FItem& g, int j) {
           const int st = issued % S;
           if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
             raise(a.err, 23, abort_flag);
             ok = false;
             return;
           }
-          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes);
-          load_a(g, kb, st);
+          const int nsub = g.nkb - C::kSub * j < C::kSub ? g.nkb - C::kSub * j : C::kSub;
+          mbar_arrive_expect_tx(full0 + 8 * st, nsub * C::kABytes1);
+          for (int u = 0; u < nsub; ++u) load_a(g, C::kSub * j + u, st, u);
           ++issued;
         };
-        const int pre = f.nkb < S ? f.nkb : S;
-        for (int kb = 0; kb < pre; ++kb) issue_w(f, kb);  // fresh stages: no wait
+        const int nst0 = (f.nkb + C::kSub - 1) / C::kSub;
+        const int pre = nst0 < S ? nst0 : S;
+        for (int j = 0; j < pre; ++j) issue_w(f, j);  // fresh stages: no wait
         griddep_wait();
         publish(item);
-        for (int kb = pre; ok && kb < f.nkb; ++kb) issue_w(f, kb);
+        for (int j = pre; ok && j < nst0; ++j) issue_w(f, j);
         while (ok && !*abort_flag) {
           item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
           if (item >= ntot) break;
           f = fdecode(a, item, C::kKB);
           publish(item);
-          for (int kb = 0; ok && kb < f.nkb; ++kb) issue_w(f, kb);
+          const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+          for (int j = 0; ok && j < nst; ++j) issue_w(f, j);
         }
       } else {
         const int pre = f.nkb < S ? f.nkb : S;
@@ -568,8 +580,10 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         const uint32_t d = tmem_base + (uint32_t)(acc * C::kAccCols);
         bool ok = true;
         if constexpr (SPLIT) {
-          for (int kb = 0; kb < f.nkb; ++kb) {
-            // the weight stage as it landed, and the activation tile once split into hi | lo
+          const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+          for (int j = 0; j < nst; ++j) {
+            // the weight stage as it landed, and the activation tiles once split into hi | lo
+            const int nsub = f.nkb - C::kSub * j < C::kSub ? f.nkb - C::kSub * j : C::kSub;
             const int st = consumed % S, sl = consumed % C::kSB;
             if (!mbar_wait(full0 + 8 * st, (consumed / S) & 1) ||
                 !mbar_wait(splitB0 + 8 * sl, (consumed / C::kSB) & 1)) {
@@ -580,8 +594,14 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             tc_fence_after();
             const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)sl * C::kBBytes);
 #pragma unroll
-            for (int k = 0; k < C::kKB / 32; ++k)
-              mma_e4m3(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+            for (int u = 0; u < C::kSub; ++u) {
+              if (u < nsub) {
+#pragma unroll
+                for (int k = 0; k < C::kKB / 32; ++k)
+                  mma_e4m3(d, sw128_desc(ab + u * C::kABytes1 + 32 * k), sw128_desc(bb + u * C::kBBytes1 + 32 * k),
+                           idesc, (j > 0) || u > 0 || k != 0);
+              }
+            }
             mma_commit(empty0 + 8 * st);
             mma_commit(emptyB0 + 8 * sl);
             ++consumed;
@@ -653,21 +673,26 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
           if (id < 0 || *abort_flag) break;
           const FItem f = fdecode(a, id, C::kKB);
           if (f.stage == 2 && !wait_stage1(a, f.s, abort_flag)) break;
-          for (int kb = 0; kb < f.nkb; ++kb) {
+          const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+          for (int j = 0; j < nst; ++j) {
             const int st = issuedB % C::kSB;
             if (!mbar_wait(emptyB0 + 8 * st, ((issuedB / C::kSB) & 1) ^ 1)) {
               raise(a.err, 37, abort_flag);
               ok = false;
               break;
             }
+            const int nsub = f.nkb - C::kSub * j < C::kSub ? f.nkb - C::kSub * j : C::kSub;
             const uint32_t bar = fullB0 + 8 * st;
-            mbar_arrive_expect_tx(bar, C::kBBytes);
-            for (int h = 0; h < C::kKB / FBK; ++h) {
-              const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + h * C::kBSub);
-              if (f.stage == 1)
-                tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
-              else
-                tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
+            mbar_arrive_expect_tx(bar, nsub * C::kBBytes1);
+            for (int u = 0; u < nsub; ++u) {
+              const int kb = C::kSub * j + u;
+              for (int h = 0; h < C::kKB / FBK; ++h) {
+                const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + (size_t)u * C::kBBytes1 + h * C::kBSub);
+                if (f.stage == 1)
+                  tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
+                else
+                  tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
+              }
             }
             ++issuedB;
           }
@@ -726,39 +751,45 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
 #pragma unroll
           for (int it = 0; it < NIT; ++it) inv[it] = pow2f(-(int)s_exp[f.s][tok[it]]);
         }
-        for (int kb = 0; kb < f.nkb; ++kb, ++kq) {
+        const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+        for (int j = 0; j < nst; ++j, ++kq) {
           const int sl = kq % C::kSB;
           if (!__all_sync(0xffffffffu, mbar_wait(fullB0 + 8 * sl, (kq / C::kSB) & 1))) {
             raise(a.err, 47, abort_flag);
             ok = false;
             break;
           }
-          // token m's bf16 rows (k 0..63 in the first 64-wide box, 64..127 in the second) are
-          // the bytes of its e4m3 rows hi = m and lo = BN + m: read all of them, then write
-          uint8_t* tile = sB + (size_t)sl * C::kBBytes;
-          uint4 v0[NIT], v1[NIT];
+          const int nsub = f.nkb - C::kSub * j < C::kSub ? f.nkb - C::kSub * j : C::kSub;
 #pragma unroll
-          for (int it = 0; it < NIT; ++it) {
-            const int m = tok[it], sw = m & 7, cc = 2 * (c & 3);
-            const uint8_t* row = tile + (c >> 2) * C::kBSub + 128 * m;
-            v0[it] = *reinterpret_cast<const uint4*>(row + 16 * (cc ^ sw));
-            v1[it] = *reinterpret_cast<const uint4*>(row + 16 * ((cc + 1) ^ sw));
-          }
-          __syncwarp();
+          for (int u = 0; u < C::kSub; ++u) {
+            if (u >= nsub) break;
+            // token m's bf16 rows (k 0..63 in the first 64-wide box, 64..127 in the second) are
+            // the bytes of its e4m3 rows hi = m and lo = BN + m: read all of them, then write
+            uint8_t* tile = sB + (size_t)sl * C::kBBytes + (size_t)u * C::kBBytes1;
+            uint4 v0[NIT], v1[NIT];
 #pragma unroll
-          for (int it = 0; it < NIT; ++it) {
-            const uint32_t w[8] = {v0[it].x, v0[it].y, v0[it].z, v0[it].w, v1[it].x, v1[it].y, v1[it].z, v1[it].w};
-            uint16_t hi[8], lo[8];
+            for (int it = 0; it < NIT; ++it) {
+              const int m = tok[it], sw = m & 7, cc = 2 * (c & 3);
+              const uint8_t* row = tile + (c >> 2) * C::kBSub + 128 * m;
+              v0[it] = *reinterpret_cast<const uint4*>(row + 16 * (cc ^ sw));
+              v1[it] = *reinterpret_cast<const uint4*>(row + 16 * ((cc + 1) ^ sw));
+            }
+            __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) split_pair(w[j], inv[it], hi[j], lo[j]);
-            uint4 H, L;
-            H.x = hi[0] | ((uint32_t)hi[1] << 16); H.y = hi[2] | ((uint32_t)hi[3] << 16);
-            H.z = hi[4] | ((uint32_t)hi[5] << 16); H.w = hi[6] | ((uint32_t)hi[7] << 16);
-            L.x = lo[0] | ((uint32_t)lo[1] << 16); L.y = lo[2] | ((uint32_t)lo[3] << 16);
-            L.z = lo[4] | ((uint32_t)lo[5] << 16); L.w = lo[6] | ((uint32_t)lo[7] << 16);
-            const int m = tok[it], off = 16 * (c ^ (m & 7));
-            *reinterpret_cast<uint4*>(tile + 128 * m + off) = H;
-            *reinterpret_cast<uint4*>(tile + 128 * (BN + m) + off) = L;
+            for (int it = 0; it < NIT; ++it) {
+              const uint32_t w[8] = {v0[it].x, v0[it].y, v0[it].z, v0[it].w, v1[it].x, v1[it].y, v1[it].z, v1[it].w};
+              uint16_t hi[8], lo[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) split_pair(w[e], inv[it], hi[e], lo[e]);
+              uint4 H, L;
+              H.x = hi[0] | ((uint32_t)hi[1] << 16); H.y = hi[2] | ((uint32_t)hi[3] << 16);
+              H.z = hi[4] | ((uint32_t)hi[5] << 16); H.w = hi[6] | ((uint32_t)hi[7] << 16);
+              L.x = lo[0] | ((uint32_t)lo[1] << 16); L.y = lo[2] | ((uint32_t)lo[3] << 16);
+              L.z = lo[4] | ((uint32_t)lo[5] << 16); L.w = lo[6] | ((uint32_t)lo[7] << 16);
+              const int m = tok[it], off = 16 * (c ^ (m & 7));
+              *reinterpret_cast<uint4*>(tile + 128 * m + off) = H;
+              *reinterpret_cast<uint4*>(tile + 128 * (BN + m) + off) = L;
+            }
           }
           fence_proxy_async_shared();
           __syncwarp();
