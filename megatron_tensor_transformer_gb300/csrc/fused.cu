@@ -65,7 +65,7 @@ constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3,
 template <int BN, bool FP8, bool SPLIT = false>
 struct FCfg {
   static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per k-block
-  static constexpr int kSub = SPLIT ? 2 : 1;               // k-blocks per stage
+  static constexpr int kSub = (SPLIT || !FP8) ? 2 : 1;     // k-blocks per stage (1: widened e4m3)
   static constexpr int kABytes1 = FP8 ? FBM * kKB : FBM * kKB * 2;  // one k-block of weights
   static constexpr int kABytes = kABytes1 * kSub;
   static constexpr int kBSub = BN * FBK * 2;               // one 64-wide activation tile
@@ -442,10 +442,10 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         else
           tma_load_3d_hint(dst, &tmA2, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
       };
-      auto load_b = [&](const FItem& f, int kb, int st) {
+      auto load_b = [&](const FItem& f, int kb, int st, int u = 0) {
         const uint32_t bar = full0 + 8 * st;
         for (int h = 0; h < C::kKB / FBK; ++h) {
-          const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + h * C::kBSub);
+          const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + (size_t)u * C::kBBytes1 + h * C::kBSub);
           if (f.stage == 1)
             tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
           else
@@ -485,33 +485,45 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
           for (int j = 0; ok && j < nst; ++j) issue_w(f, j);
         }
       } else {
-        const int pre = f.nkb < S ? f.nkb : S;
-        for (int kb = 0; kb < pre; ++kb) {
-          mbar_expect_tx(full0 + 8 * kb, C::kABytes);
-          load_a(f, kb, kb);
+        // bf16: a stage holds kSub k-blocks of weights and their activation tiles (the item's last
+        // stage may hold fewer)
+        auto nsub_of = [&](const FItem& g, int j) {
+          return g.nkb - C::kSub * j < C::kSub ? g.nkb - C::kSub * j : C::kSub;
+        };
+        auto issue_ab = [&](const FItem& g, int j, int code) {  // stage j: weights and activations
+          const int st = issued % S;
+          if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
+            raise(a.err, code, abort_flag);
+            ok = false;
+            return;
+          }
+          const int nsub = nsub_of(g, j);
+          mbar_arrive_expect_tx(full0 + 8 * st, nsub * (C::kABytes1 + C::kBBytes1));
+          for (int u = 0; u < nsub; ++u) {
+            load_a(g, C::kSub * j + u, st, u);
+            load_b(g, C::kSub * j + u, st, u);
+          }
+          ++issued;
+        };
+        const int nst0 = (f.nkb + C::kSub - 1) / C::kSub;
+        const int pre = nst0 < S ? nst0 : S;
+        for (int j = 0; j < pre; ++j) {
+          const int nsub = nsub_of(f, j);
+          mbar_expect_tx(full0 + 8 * j, nsub * C::kABytes1);
+          for (int u = 0; u < nsub; ++u) load_a(f, C::kSub * j + u, j, u);
         }
         griddep_wait();
         publish(item);
         if (ok && f.stage == 2) ok = wait_stage1(a, f.s, abort_flag);
         if (ok) {
-          for (int kb = 0; kb < pre; ++kb) {
-            mbar_arrive_expect_tx(full0 + 8 * kb, C::kBBytes);
-            load_b(f, kb, kb);
+          for (int j = 0; j < pre; ++j) {
+            const int nsub = nsub_of(f, j);
+            mbar_arrive_expect_tx(full0 + 8 * j, nsub * C::kBBytes1);
+            for (int u = 0; u < nsub; ++u) load_b(f, C::kSub * j + u, j, u);
           }
           issued = pre;
         }
-        for (int kb = pre; ok && kb < f.nkb; ++kb) {
-          const int st = issued % S;
-          if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
-            raise(a.err, 23, abort_flag);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-          load_a(f, kb, st);
-          load_b(f, kb, st);
-          ++issued;
-        }
+        for (int j = pre; ok && j < nst0; ++j) issue_ab(f, j, 23);
         // then items from the shared counter, in order: stage 1 of every shard, then stage 2
         while (ok && !*abort_flag) {
           item = (int)gridDim.x + (int)atomicAdd(a.sync + kSyncItem, 1u);
@@ -519,39 +531,33 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
           f = fdecode(a, item, C::kKB);
           publish(item);
           if (!ok) break;
-          int kb = 0;
+          const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+          int j = 0;
           if (f.stage == 2 && ld_acquire(a.sync + kSyncDone + f.s) < (unsigned)(a.rows1 / FBM)) {
             // weights ahead (their stages were freed by earlier items), then the activations
-            const int la = f.nkb < S ? f.nkb : S;
-            for (; kb < la; ++kb) {
+            const int la = nst < S ? nst : S;
+            for (; j < la; ++j) {
               const int st = issued % S;
               if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
                 raise(a.err, 24, abort_flag);
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-              load_a(f, kb, st);
+              const int nsub = nsub_of(f, j);
+              mbar_arrive_expect_tx(full0 + 8 * st, nsub * (C::kABytes1 + C::kBBytes1));
+              for (int u = 0; u < nsub; ++u) load_a(f, C::kSub * j + u, st, u);
               ++issued;
             }
             if (ok) ok = wait_stage1(a, f.s, abort_flag);
             if (!ok) break;
-            for (int j = 0; j < la; ++j) load_b(f, j, (issued - la + j) % S);
+            for (int i = 0; i < la; ++i) {
+              const int nsub = nsub_of(f, i);
+              for (int u = 0; u < nsub; ++u) load_b(f, C::kSub * i + u, (issued - la + i) % S, u);
+            }
           } else if (f.stage == 2) {
             fence_proxy_async_global();
           }
-          for (; kb < f.nkb; ++kb) {
-            const int st = issued % S;
-            if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
-              raise(a.err, 25, abort_flag);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
-            load_a(f, kb, st);
-            load_b(f, kb, st);
-            ++issued;
-          }
+          for (; ok && j < nst; ++j) issue_ab(f, j, 25);
         }
       }
       if (ok) publish(-1);
@@ -607,7 +613,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             ++consumed;
           }
         } else {
-          for (int kb = 0; kb < f.nkb; ++kb) {
+          const int nst = (f.nkb + C::kSub - 1) / C::kSub;
+          for (int kb = 0; kb < nst; ++kb) {
             // the activation tile: in the weight stage (bf16), or in its own ring (e4m3)
             constexpr int NB = FP8 ? C::kSB : S;
             const int st = consumed % NB;
@@ -636,9 +643,16 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             } else {
               tc_fence_after();
               const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes);
+              const int nsub = f.nkb - C::kSub * kb < C::kSub ? f.nkb - C::kSub * kb : C::kSub;
 #pragma unroll
-              for (int k = 0; k < FBK / 16; ++k)
-                mma_bf16(d, sw128_desc(ab + 32 * k), sw128_desc(bb + 32 * k), idesc, (kb > 0) || k != 0);
+              for (int u = 0; u < C::kSub; ++u) {
+                if (u < nsub) {
+#pragma unroll
+                  for (int k = 0; k < FBK / 16; ++k)
+                    mma_bf16(d, sw128_desc(ab + u * C::kABytes1 + 32 * k), sw128_desc(bb + u * C::kBBytes1 + 32 * k),
+                             idesc, (kb > 0) || u > 0 || k != 0);
+                }
+              }
               mma_commit(empty0 + 8 * st);
             }
             ++consumed;
