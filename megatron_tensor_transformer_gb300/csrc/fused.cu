@@ -74,9 +74,10 @@ struct FCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   // activation ring (e4m3 only)
   // split: a slot is refilled only after the MMA has read it, and its tile then takes an L2 round
-  // trip and the split before the MMA can use it, so the ring must cover that whole loop
-  static constexpr int kSB = SPLIT ? (kBBytes <= 8192 ? 8 : (kBBytes <= 16384 ? 4 : 3))
-                                   : (FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0);
+  // trip and the split before the MMA can use it (about two stages' time), so the ring must cover
+  // that loop; the rest of the shared memory holds weight stages, whose round trip from HBM is
+  // several stages long
+  static constexpr int kSB = SPLIT ? (kBBytes <= 16384 ? 4 : 3) : (FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0);
   static constexpr int kMaxStages = SPLIT ? 6 : (FP8 ? 10 : 8);
   // split: no tensor-memory A slots to feed, so more of the 227 KB goes to weights in flight
   static constexpr int kRingBytes = (SPLIT ? 224 : 200) * 1024 - kSB * kBBytes;
@@ -123,6 +124,14 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 }
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Thread 0, after a barrier of the epilogue warps: one GPU-scope acquire-release add.  The
+// release covers the stores the barrier ordered before it (the other threads' partials or y);
+// the acquire lets the CTA read, after the next barrier, what the earlier arrivals released.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
 }
 // Generic-proxy global writes (h, o_in) are read by other CTAs' TMA (async proxy).
 __device__ __forceinline__ void fence_proxy_async_global() {
@@ -316,8 +325,26 @@ __device__ __forceinline__ void input_norm(const FusedArgs& a) {
   const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
   for (int m = w; m < a.M; m += 4) {
     float ss = 0.f;
-    for (int k = 8 * l; k < a.d; k += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)m * a.d + k);
+    const __nv_bfloat16* xr = a.x + (size_t)m * a.d;
+    int k = 8 * l;
+    // eight 16-byte loads in flight, then the squares in k order
+    for (; k + 7 * 256 < a.d; k += 8 * 256) {
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = *reinterpret_cast<const uint4*>(xr + k + i * 256);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float e0 = bf16_lo(u[j]), e1 = bf16_hi(u[j]);
+          ss += e0 * e0;
+          ss += e1 * e1;
+        }
+      }
+    }
+    for (; k < a.d; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(xr + k);
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -973,17 +1000,18 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
       ++it;
       // make this item's stores visible, then count it (stage 1) or take the tile's ticket (stage 2)
-      __threadfence();
-      if (f.stage == 1) fence_proxy_async_global();
-      epi_bar();
       if (f.stage == 1) {
+        // h / o_in are read by other CTAs' TMA loads (the async proxy)
+        __threadfence();
+        fence_proxy_async_global();
+        epi_bar();
         if (threadIdx.x == 0) red_release_add(a.sync + kSyncDone + f.s, 1u);
       } else {
+        epi_bar();
         if (threadIdx.x == 0) {
-          const unsigned old = atomicAdd(a.sync + kSyncTicket + f.rt, 1u);
+          const unsigned old = atom_add_acq_rel(a.sync + kSyncTicket + f.rt, 1u);
           const int last = old == (unsigned)(a.t - 1);
           if (last) a.sync[kSyncTicket + f.rt] = 0u;  // every shard has arrived: reset for the next launch
-          __threadfence();
           *last_flag = last;
         }
         epi_bar();
@@ -991,21 +1019,29 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
           fold_tile<FP8 ? 2 : 3>(a, f.rt);
           if (a.out_rms) {
             // the tile whose fold comes last sums every tile's share, in tile order
-            __threadfence();
             epi_bar();
             if (threadIdx.x == 0) {
               const int nt = a.d / FBM;
-              const unsigned old = atomicAdd(a.sync + kSyncNormTiles, 1u);
+              const unsigned old = atom_add_acq_rel(a.sync + kSyncNormTiles, 1u);
               const int lastn = old == (unsigned)(nt - 1);
               if (lastn) a.sync[kSyncNormTiles] = 0u;
-              __threadfence();
               *norm_last = lastn;
             }
             epi_bar();
             if (*norm_last && threadIdx.x < a.M) {
               const int nt = a.d / FBM;
+              const float* row = a.norm_ss + (size_t)threadIdx.x * nt;
+              // 16 loads in flight, then the adds in tile order
               float ss = 0.f;
-              for (int t2 = 0; t2 < nt; ++t2) ss += __ldcg(a.norm_ss + (size_t)threadIdx.x * nt + t2);
+              int t2 = 0;
+              for (; t2 + 16 <= nt; t2 += 16) {
+                float v[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) v[j] = __ldcg(row + t2 + j);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) ss += v[j];
+              }
+              for (; t2 < nt; ++t2) ss += __ldcg(row + t2);
               a.out_rms[threadIdx.x] = 1.f / sqrtf(ss / (float)a.d + a.eps);
             }
           }
