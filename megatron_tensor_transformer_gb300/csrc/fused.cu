@@ -461,13 +461,11 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         mbar_arrive(ifull0 + 8 * r);
         ++q;
       };
-      // k-block kb of item f into sub-block u of stage st
-      auto load_a = [&](const FItem& f, int kb, int st, int u = 0) {
-        const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes + (size_t)u * C::kABytes1), bar = full0 + 8 * st;
-        if (f.stage == 1)
-          tma_load_3d_hint(dst, &tmA1, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
-        else
-          tma_load_3d_hint(dst, &tmA2, kb * C::kKB, f.rt * FBM, f.s, bar, pol_w);
+      // the weights of stage j of item f (k-blocks kSub j ..) into ring stage st: one TMA copy of
+      // kABytes (a k-block past the item's last reads as zeros and is not multiplied)
+      auto load_w = [&](const FItem& f, int j, int st) {
+        const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes), bar = full0 + 8 * st;
+        tma_load_4d_hint(dst, f.stage == 1 ? &tmA1 : &tmA2, 0, f.rt * FBM, C::kSub * j, f.s, bar, pol_w);
       };
       auto load_b = [&](const FItem& f, int kb, int st, int u = 0) {
         const uint32_t bar = full0 + 8 * st;
@@ -492,9 +490,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             ok = false;
             return;
           }
-          const int nsub = g.nkb - C::kSub * j < C::kSub ? g.nkb - C::kSub * j : C::kSub;
-          mbar_arrive_expect_tx(full0 + 8 * st, nsub * C::kABytes1);
-          for (int u = 0; u < nsub; ++u) load_a(g, C::kSub * j + u, st, u);
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes);
+          load_w(g, j, st);
           ++issued;
         };
         const int nst0 = (f.nkb + C::kSub - 1) / C::kSub;
@@ -525,19 +522,16 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             return;
           }
           const int nsub = nsub_of(g, j);
-          mbar_arrive_expect_tx(full0 + 8 * st, nsub * (C::kABytes1 + C::kBBytes1));
-          for (int u = 0; u < nsub; ++u) {
-            load_a(g, C::kSub * j + u, st, u);
-            load_b(g, C::kSub * j + u, st, u);
-          }
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + nsub * C::kBBytes1);
+          load_w(g, j, st);
+          for (int u = 0; u < nsub; ++u) load_b(g, C::kSub * j + u, st, u);
           ++issued;
         };
         const int nst0 = (f.nkb + C::kSub - 1) / C::kSub;
         const int pre = nst0 < S ? nst0 : S;
         for (int j = 0; j < pre; ++j) {
-          const int nsub = nsub_of(f, j);
-          mbar_expect_tx(full0 + 8 * j, nsub * C::kABytes1);
-          for (int u = 0; u < nsub; ++u) load_a(f, C::kSub * j + u, j, u);
+          mbar_expect_tx(full0 + 8 * j, C::kABytes);
+          load_w(f, j, j);
         }
         griddep_wait();
         publish(item);
@@ -570,9 +564,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
                 ok = false;
                 break;
               }
-              const int nsub = nsub_of(f, j);
-              mbar_arrive_expect_tx(full0 + 8 * st, nsub * (C::kABytes1 + C::kBBytes1));
-              for (int u = 0; u < nsub; ++u) load_a(f, C::kSub * j + u, st, u);
+              mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + nsub_of(f, j) * C::kBBytes1);
+              load_w(f, j, st);
               ++issued;
             }
             if (ok) ok = wait_stage1(a, f.s, abort_flag);
@@ -1112,12 +1105,16 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tm[4];
-  const cuuint32_t es3[3] = {1, 1, 1}, es2[2] = {1, 1};
-  {  // stage-1 weights {K1 = d, rows1, t}
-    const cuuint64_t dims[3] = {(cuuint64_t)a.d, (cuuint64_t)a.rows1, (cuuint64_t)a.t};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.d * wes, (cuuint64_t)a.stride1};
-    const cuuint32_t box[3] = {(cuuint32_t)C::kKB, FBM, 1};
-    if (enc(&tm[0], wty, 3, const_cast<uint8_t*>(a.w1), dims, strides, box, es3,
+  const cuuint32_t es4[4] = {1, 1, 1, 1}, es2[2] = {1, 1};
+  // Weights as {k within a k-block, row, k-block, shard}: one copy brings a whole stage, kSub
+  // consecutive k-blocks of 128 rows, as kSub 128-row tiles one after another in shared memory.
+  // A TMA copy costs each SM about the same time whatever its size, so two 16 KB boxes per stage
+  // capped an SM's weight stream near half of what one 32 KB copy reaches.
+  {  // stage-1 weights [t][rows1][d]
+    const cuuint64_t dims[4] = {(cuuint64_t)C::kKB, (cuuint64_t)a.rows1, (cuuint64_t)(a.d / C::kKB), (cuuint64_t)a.t};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.d * wes, (cuuint64_t)C::kKB * wes, (cuuint64_t)a.stride1};
+    const cuuint32_t box[4] = {(cuuint32_t)C::kKB, FBM, (cuuint32_t)C::kSub, 1};
+    if (enc(&tm[0], wty, 4, const_cast<uint8_t*>(a.w1), dims, strides, box, es4,
             CU_TENSOR_MAP_INTERLEAVE_NONE, wsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -1131,11 +1128,11 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
-  {  // stage-2 weights {K2, rows2 = d, t}
-    const cuuint64_t dims[3] = {(cuuint64_t)a.K2, (cuuint64_t)a.d, (cuuint64_t)a.t};
-    const cuuint64_t strides[2] = {(cuuint64_t)a.K2 * wes, (cuuint64_t)a.stride2};
-    const cuuint32_t box[3] = {(cuuint32_t)C::kKB, FBM, 1};
-    if (enc(&tm[2], wty, 3, const_cast<uint8_t*>(a.w2), dims, strides, box, es3,
+  {  // stage-2 weights [t][rows2 = d][K2]
+    const cuuint64_t dims[4] = {(cuuint64_t)C::kKB, (cuuint64_t)a.d, (cuuint64_t)(a.K2 / C::kKB), (cuuint64_t)a.t};
+    const cuuint64_t strides[3] = {(cuuint64_t)a.K2 * wes, (cuuint64_t)C::kKB * wes, (cuuint64_t)a.stride2};
+    const cuuint32_t box[4] = {(cuuint32_t)C::kKB, FBM, (cuuint32_t)C::kSub, 1};
+    if (enc(&tm[2], wty, 4, const_cast<uint8_t*>(a.w2), dims, strides, box, es4,
             CU_TENSOR_MAP_INTERLEAVE_NONE, wsw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
