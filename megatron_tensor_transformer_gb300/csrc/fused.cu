@@ -93,6 +93,7 @@ struct FCfg {
   static constexpr int kThreads = 192 + 32 * kConvWarps + (FP8 ? 32 : 0);
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kABytes + (size_t)kBSlots * kBBytes + 1024;
   static_assert(!SPLIT || (FP8 && BN % 8 == 0), "split activations: e4m3 weights, 8-token multiples");
+  static_assert(!SPLIT || kSB <= kStages, "split activation slots are freed through the weight stages' barriers");
 };
 
 struct FItem {
@@ -628,8 +629,9 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
                            idesc, (j > 0) || u > 0 || k != 0);
               }
             }
+            // one commit frees the weight stage and (the activation producer waits on the same
+            // barrier) the activation slot
             mma_commit(empty0 + 8 * st);
-            mma_commit(emptyB0 + 8 * sl);
             ++consumed;
           }
         } else {
@@ -710,7 +712,14 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
           const int nst = (f.nkb + C::kSub - 1) / C::kSub;
           for (int j = 0; j < nst; ++j) {
             const int st = issuedB % C::kSB;
-            if (!mbar_wait(emptyB0 + 8 * st, ((issuedB / C::kSB) & 1) ^ 1)) {
+            // the slot's previous tile (stage issuedB - kSB) has been read once the MMAs of that
+            // stage are done: split activations have no commit of their own, the stage's weight
+            // barrier tells (it cannot complete a later phase first while kSB <= kStages)
+            const bool freed =
+                SPLIT ? (issuedB < C::kSB ||
+                         mbar_wait(empty0 + 8 * ((issuedB - C::kSB) % S), ((issuedB - C::kSB) / S) & 1))
+                      : mbar_wait(emptyB0 + 8 * st, ((issuedB / C::kSB) & 1) ^ 1);
+            if (!freed) {
               raise(a.err, 37, abort_flag);
               ok = false;
               break;
