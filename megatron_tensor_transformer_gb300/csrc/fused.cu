@@ -360,6 +360,19 @@ __device__ __forceinline__ void input_norm(const FusedArgs& a) {
   }
 }
 
+// The activation tiles of stage j of item f: one TMA copy of kBBytes, the stage's 64-column chunks
+// (kSub k-blocks) as [chunk][BN tokens][128 B] tiles.  x (stage 1) and h / o_in (stage 2) are
+// viewed as {64 columns, token, chunk}; a chunk past the item's last k-block is not multiplied.
+template <class C>
+__device__ __forceinline__ void load_act_stage(const CUtensorMap* tmB1, const CUtensorMap* tmB2, const FusedArgs& a,
+                                               const FItem& f, int j, uint32_t dst, uint32_t bar, uint64_t pol) {
+  const int c0 = C::kSub * j * (C::kKB / FBK);
+  if (f.stage == 1)
+    tma_load_3d_hint(dst, tmB1, 0, 0, c0, bar, pol);
+  else
+    tma_load_3d_hint(dst, tmB2, 0, 0, f.s * (a.K2 / FBK) + c0, bar, pol);
+}
+
 template <int BN, int KIND, bool FP8, bool SPLIT>
 __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
     fused_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmB1,
@@ -468,15 +481,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         const uint32_t dst = smem_u32(sA + (size_t)st * C::kABytes), bar = full0 + 8 * st;
         tma_load_4d_hint(dst, f.stage == 1 ? &tmA1 : &tmA2, 0, f.rt * FBM, C::kSub * j, f.s, bar, pol_w);
       };
-      auto load_b = [&](const FItem& f, int kb, int st, int u = 0) {
-        const uint32_t bar = full0 + 8 * st;
-        for (int h = 0; h < C::kKB / FBK; ++h) {
-          const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + (size_t)u * C::kBBytes1 + h * C::kBSub);
-          if (f.stage == 1)
-            tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
-          else
-            tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
-        }
+      auto load_x = [&](const FItem& f, int j, int st) {  // bf16: the activations of stage j into stage st
+        load_act_stage<C>(&tmB1, &tmB2, a, f, j, smem_u32(sB + (size_t)st * C::kBBytes), full0 + 8 * st, pol_x);
       };
       // first item (static): its first stages of weights go out before the previous kernel ends
       int item = blockIdx.x;
@@ -512,9 +518,6 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       } else {
         // bf16: a stage holds kSub k-blocks of weights and their activation tiles (the item's last
         // stage may hold fewer)
-        auto nsub_of = [&](const FItem& g, int j) {
-          return g.nkb - C::kSub * j < C::kSub ? g.nkb - C::kSub * j : C::kSub;
-        };
         auto issue_ab = [&](const FItem& g, int j, int code) {  // stage j: weights and activations
           const int st = issued % S;
           if (!mbar_wait(empty0 + 8 * st, ((issued / S) & 1) ^ 1)) {
@@ -522,10 +525,9 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
             ok = false;
             return;
           }
-          const int nsub = nsub_of(g, j);
-          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + nsub * C::kBBytes1);
+          mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
           load_w(g, j, st);
-          for (int u = 0; u < nsub; ++u) load_b(g, C::kSub * j + u, st, u);
+          load_x(g, j, st);
           ++issued;
         };
         const int nst0 = (f.nkb + C::kSub - 1) / C::kSub;
@@ -539,9 +541,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         if (ok && f.stage == 2) ok = wait_stage1(a, f.s, abort_flag);
         if (ok) {
           for (int j = 0; j < pre; ++j) {
-            const int nsub = nsub_of(f, j);
-            mbar_arrive_expect_tx(full0 + 8 * j, nsub * C::kBBytes1);
-            for (int u = 0; u < nsub; ++u) load_b(f, C::kSub * j + u, j, u);
+            mbar_arrive_expect_tx(full0 + 8 * j, C::kBBytes);
+            load_x(f, j, j);
           }
           issued = pre;
         }
@@ -565,16 +566,13 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
                 ok = false;
                 break;
               }
-              mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + nsub_of(f, j) * C::kBBytes1);
+              mbar_arrive_expect_tx(full0 + 8 * st, C::kABytes + C::kBBytes);
               load_w(f, j, st);
               ++issued;
             }
             if (ok) ok = wait_stage1(a, f.s, abort_flag);
             if (!ok) break;
-            for (int i = 0; i < la; ++i) {
-              const int nsub = nsub_of(f, i);
-              for (int u = 0; u < nsub; ++u) load_b(f, C::kSub * i + u, (issued - la + i) % S, u);
-            }
+            for (int i = 0; i < la; ++i) load_x(f, i, (issued - la + i) % S);
           } else if (f.stage == 2) {
             fence_proxy_async_global();
           }
@@ -724,19 +722,9 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
               ok = false;
               break;
             }
-            const int nsub = f.nkb - C::kSub * j < C::kSub ? f.nkb - C::kSub * j : C::kSub;
             const uint32_t bar = fullB0 + 8 * st;
-            mbar_arrive_expect_tx(bar, nsub * C::kBBytes1);
-            for (int u = 0; u < nsub; ++u) {
-              const int kb = C::kSub * j + u;
-              for (int h = 0; h < C::kKB / FBK; ++h) {
-                const uint32_t dst = smem_u32(sB + (size_t)st * C::kBBytes + (size_t)u * C::kBBytes1 + h * C::kBSub);
-                if (f.stage == 1)
-                  tma_load_2d_hint(dst, &tmB1, kb * C::kKB + h * FBK, 0, bar, pol_x);
-                else
-                  tma_load_2d_hint(dst, &tmB2, f.s * a.K2 + kb * C::kKB + h * FBK, 0, bar, pol_x);
-              }
-            }
+            mbar_arrive_expect_tx(bar, C::kBBytes);
+            load_act_stage<C>(&tmB1, &tmB2, a, f, j, smem_u32(sB + (size_t)st * C::kBBytes), bar, pol_x);
             ++issuedB;
           }
         }
@@ -1114,7 +1102,7 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
   EncodeTiled enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   CUtensorMap tm[4];
-  const cuuint32_t es4[4] = {1, 1, 1, 1}, es2[2] = {1, 1};
+  const cuuint32_t es4[4] = {1, 1, 1, 1}, es3[3] = {1, 1, 1};
   // Weights as {k within a k-block, row, k-block, shard}: one copy brings a whole stage, kSub
   // consecutive k-blocks of 128 rows, as kSub 128-row tiles one after another in shared memory.
   // A TMA copy costs each SM about the same time whatever its size, so two 16 KB boxes per stage
@@ -1128,11 +1116,13 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // Activations as {64 columns, token, 64-column chunk}: one copy brings a stage's chunks.
+  constexpr cuuint32_t kChunks = (cuuint32_t)(C::kKB / FBK * C::kSub);
   {  // x [M, d]
-    const cuuint64_t dims[2] = {(cuuint64_t)a.d, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.d * 2};
-    const cuuint32_t box[2] = {FBK, BN};
-    if (enc(&tm[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), dims, strides, box, es2,
+    const cuuint64_t dims[3] = {(cuuint64_t)FBK, (cuuint64_t)a.M, (cuuint64_t)(a.d / FBK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.d * 2, (cuuint64_t)FBK * 2};
+    const cuuint32_t box[3] = {FBK, BN, kChunks};
+    if (enc(&tm[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<__nv_bfloat16*>(a.x), dims, strides, box, es3,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
@@ -1147,10 +1137,10 @@ static cudaError_t fused_go(const FusedArgs& a, cudaStream_t st, bool pdl) {
       return cudaErrorInvalidValue;
   }
   {  // stage-2 activations [M, t*K2] (h or o_in)
-    const cuuint64_t dims[2] = {(cuuint64_t)a.t * a.K2, (cuuint64_t)a.M};
-    const cuuint64_t strides[1] = {(cuuint64_t)a.t * a.K2 * 2};
-    const cuuint32_t box[2] = {FBK, BN};
-    if (enc(&tm[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a.mid2, dims, strides, box, es2,
+    const cuuint64_t dims[3] = {(cuuint64_t)FBK, (cuuint64_t)a.M, (cuuint64_t)(a.t * a.K2 / FBK)};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.t * a.K2 * 2, (cuuint64_t)FBK * 2};
+    const cuuint32_t box[3] = {FBK, BN, kChunks};
+    if (enc(&tm[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, a.mid2, dims, strides, box, es3,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
