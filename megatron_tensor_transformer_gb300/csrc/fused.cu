@@ -617,14 +617,16 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes), bb = smem_u32(sB + (size_t)sl * C::kBBytes);
+            // the stage's descriptors once; an offset inside the stage adds to the address field
+            const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)st * C::kABytes)),
+                           bd = sw128_desc(smem_u32(sB + (size_t)sl * C::kBBytes));
 #pragma unroll
             for (int u = 0; u < C::kSub; ++u) {
               if (u < nsub) {
 #pragma unroll
                 for (int k = 0; k < C::kKB / 32; ++k)
-                  mma_e4m3(d, sw128_desc(ab + u * C::kABytes1 + 32 * k), sw128_desc(bb + u * C::kBBytes1 + 32 * k),
-                           idesc, (j > 0) || u > 0 || k != 0);
+                  mma_e4m3(d, ad + desc_off(u * C::kABytes1 + 32 * k), bd + desc_off(u * C::kBBytes1 + 32 * k), idesc,
+                           (j > 0) || u > 0 || k != 0);
               }
             }
             // one commit frees the weight stage and (the activation producer waits on the same
@@ -662,15 +664,15 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
               mma_commit(aempty0 + 8 * slot);
             } else {
               tc_fence_after();
-              const uint32_t ab = smem_u32(sA + (size_t)st * C::kABytes);
+              const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)st * C::kABytes)), bd = sw128_desc(bb);
               const int nsub = f.nkb - C::kSub * kb < C::kSub ? f.nkb - C::kSub * kb : C::kSub;
 #pragma unroll
               for (int u = 0; u < C::kSub; ++u) {
                 if (u < nsub) {
 #pragma unroll
                   for (int k = 0; k < FBK / 16; ++k)
-                    mma_bf16(d, sw128_desc(ab + u * C::kABytes1 + 32 * k), sw128_desc(bb + u * C::kBBytes1 + 32 * k),
-                             idesc, (kb > 0) || u > 0 || k != 0);
+                    mma_bf16(d, ad + desc_off(u * C::kABytes1 + 32 * k), bd + desc_off(u * C::kBBytes1 + 32 * k), idesc,
+                             (kb > 0) || u > 0 || k != 0);
                 }
               }
               mma_commit(empty0 + 8 * st);

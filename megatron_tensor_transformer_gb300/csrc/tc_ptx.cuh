@@ -220,6 +220,10 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
+// The same descriptor for an address `bytes` further on: the address field holds address / 16 in 14
+// bits, and shared-memory addresses stay below 256 KB, so the sum cannot carry out of the field.
+__host__ __device__ constexpr uint64_t desc_off(uint32_t bytes) { return (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
