@@ -79,14 +79,18 @@ struct FCfg {
   // several stages long
   static constexpr int kSB = SPLIT ? (kBBytes <= 16384 ? 4 : 3) : (FP8 ? (kBBytes <= 8192 ? 8 : 4) : 0);
   static constexpr int kMaxStages = SPLIT ? 6 : (FP8 ? 10 : 8);
-  // split: no tensor-memory A slots to feed, so more of the 227 KB goes to weights in flight
-  static constexpr int kRingBytes = (SPLIT ? 224 : 200) * 1024 - kSB * kBBytes;
+  // bf16 and split: no tensor-memory A slots to feed, so more of the 227 KB goes to weights in flight
+  static constexpr int kRingBytes = ((FP8 && !SPLIT) ? 200 : 224) * 1024 - kSB * kBBytes;
   static constexpr int kUnitBytes = FP8 ? kABytes : kStageBytes;
   static constexpr int kStages = kRingBytes / kUnitBytes > kMaxStages ? kMaxStages : kRingBytes / kUnitBytes;
   static constexpr int kBSlots = FP8 ? kSB : kStages;  // activation tiles held in shared memory
   static constexpr int kASlots = 6, kACol0 = 128, kASlotCols = kKB / 2;
   static constexpr int kAccCols = SPLIT ? 2 * BN : BN;  // accumulator columns (hi and lo halves)
-  static constexpr int kTmemCols = SPLIT ? (4 * BN < 32 ? 32 : 4 * BN) : (FP8 ? 512 : (2 * BN < 32 ? 32 : 2 * BN));
+  // accumulators in flight: the next item's MMAs run while the epilogue drains the last one
+  // (four measured slower than two for the hi/lo block); the widened e4m3 path keeps the rest of
+  // its tensor memory for the A slots
+  static constexpr int kAcc = 2;
+  static constexpr int kTmemCols = (FP8 && !SPLIT) ? 512 : (kAcc * kAccCols < 32 ? 32 : kAcc * kAccCols);
   static constexpr int kConvWarps = FP8 ? (SPLIT ? 4 : 8) : 0;
   // converter warps from warp 6; e4m3: then the activation producer
   static constexpr int kProducerB = 6 + kConvWarps;
@@ -386,9 +390,10 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
   uint8_t* sA = smem;                            // S x [128 rows x 64] weights (bf16 SW128 or e4m3 SW64)
   uint8_t* sB = smem + (size_t)S * C::kABytes;   // kBSlots x [BN rows x kKB] bf16, SW128 tiles of 64
   uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)C::kBSlots * C::kBBytes);
-  // bars: full[S], empty[S], tfull[2], tempty[2], ifull[kRing], iempty[kRing], drain, afull[kASlots],
+  // bars: full[S], empty[S], tfull[kAcc], tempty[kAcc], ifull[kRing], iempty[kRing], drain, afull[kASlots],
   // aempty[kASlots], fullB[kSB], emptyB[kSB], (split activations) splitB[kSB]
-  int* ring = reinterpret_cast<int*>(bars + 2 * S + 4 + 2 * kRing + 1 + 2 * C::kASlots + 2 * C::kSB + kSplitBars);
+  constexpr int kAcc = C::kAcc;
+  int* ring = reinterpret_cast<int*>(bars + 2 * S + 2 * kAcc + 2 * kRing + 1 + 2 * C::kASlots + 2 * C::kSB + kSplitBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ring + kRing);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* mma_consumed = reinterpret_cast<int*>(tmem_slot + 2);
@@ -396,8 +401,9 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
   int* conv_consumed = reinterpret_cast<int*>(tmem_slot + 4);  // e4m3: weight stages the converters took
   volatile int* norm_last = reinterpret_cast<volatile int*>(tmem_slot + 5);
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), tfull0 = smem_u32(bars + 2 * S),
-                 tempty0 = smem_u32(bars + 2 * S + 2), ifull0 = smem_u32(bars + 2 * S + 4),
-                 iempty0 = smem_u32(bars + 2 * S + 4 + kRing), drain_bar = smem_u32(bars + 2 * S + 4 + 2 * kRing),
+                 tempty0 = smem_u32(bars + 2 * S + kAcc), ifull0 = smem_u32(bars + 2 * S + 2 * kAcc),
+                 iempty0 = smem_u32(bars + 2 * S + 2 * kAcc + kRing),
+                 drain_bar = smem_u32(bars + 2 * S + 2 * kAcc + 2 * kRing),
                  afull0 = drain_bar + 8, aempty0 = drain_bar + 8 + 8 * C::kASlots,
                  fullB0 = aempty0 + 8 * C::kASlots, emptyB0 = fullB0 + 8 * C::kSB, splitB0 = emptyB0 + 8 * C::kSB;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -415,7 +421,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       // e4m3 widened: freed by the converters; otherwise by the MMA's commit
       mbar_init(empty0 + 8 * i, FP8 && !SPLIT ? C::kConvWarps : 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kAcc; ++i) {
       mbar_init(tfull0 + 8 * i, 1);
       mbar_init(tempty0 + 8 * i, 4);  // one arrival per epilogue warp
     }
@@ -596,8 +602,8 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
         ++q;
         if (id < 0) break;
         const FItem f = fdecode(a, id, C::kKB);
-        const int acc = it & 1;
-        if (!mbar_wait(tempty0 + 8 * acc, ((it >> 1) & 1) ^ 1)) {
+        const int acc = it % kAcc;
+        if (!mbar_wait(tempty0 + 8 * acc, ((it / kAcc) & 1) ^ 1)) {
           raise(a.err, 27, abort_flag);
           break;
         }
@@ -919,7 +925,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
       ++q;
       if (id < 0 || __any_sync(0xffffffffu, *abort_flag != 0)) break;
       const FItem f = fdecode(a, id, C::kKB);
-      const int acc = it & 1;
+      const int acc = it % kAcc;
       // fetched while the item's MMAs run: the row's fp32 scale (e4m3), and (split activations)
       // the first 16 tokens' scales 2^e
       const int p = f.rt * FBM + r;
@@ -936,7 +942,7 @@ __global__ void __launch_bounds__(FCfg<BN, FP8, SPLIT>::kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 16; ++j) tsc0[j] = j < a.M ? pow2f(split_exp_bits(split_max + j)) : 0.f;
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it >> 1) & 1))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull0 + 8 * acc, (it / kAcc) & 1))) {
         raise(a.err, 31, abort_flag);
         break;
       }
