@@ -221,3 +221,24 @@ def test_fused_fp8_blocks_vs_oracle(dev, t, M, flags):
     qkv, qkv_ref, y, y_ref = _fp8_proj(1024, 16, 8, 64, t, M, dev, seed=14, flags=flags)
     check_close(bits(qkv), qkv_ref, what=f"fused fp8 qkv t={t} M={M}")
     check_close(bits(y), y_ref, what=f"fused fp8 o_proj t={t} M={M}")
+
+
+@pytest.mark.parametrize("wtype,d,ffn,t,M", [(tpx.TP_BF16, 256, 1536, 8, 5), (tpx.TP_BF16, 256, 1536, 8, 16),
+                                             (FP8, 384, 1536, 4, 16), (FP8, 384, 1536, 4, 33)],
+                         ids=["bf16-M5", "bf16-M16", "e4m3-M16", "e4m3-M33"])
+def test_fused_blocks_half_full_last_stage(dev, wtype, d, ffn, t, M):
+    """A pipeline stage carries two k-blocks in one copy of weights and one of activations.
+    These shapes leave an item's last stage half full: bf16 with 3 row-parallel k-blocks of 64,
+    e4m3 (hi/lo, the default) with 3 k-blocks of 128 in both halves and in the attention block's
+    column-parallel half.  The k-block past the item's end (zeros, or the next shard's
+    activations) must not reach the products."""
+    m = Mlp(d, ffn, t, M, dev, seed=31, wtype=wtype)
+    for res in (True, False):
+        y, h = m.run(residual=res)
+        y_ref, h_ref = m.oracle(residual=res)
+        check_close(bits(y), y_ref, what=f"MLP d={d} ffn={ffn} t={t} M={M} res={res}")
+        check_h(bits(h), h_ref, what=f"h d={d} t={t} M={M}")
+    if wtype == FP8:
+        qkv, qkv_ref, y, y_ref = _fp8_proj(d, 8, 4, 64, 2, M, dev, seed=32)
+        check_close(bits(qkv), qkv_ref, what=f"qkv d={d} M={M}")
+        check_close(bits(y), y_ref, what=f"o_proj d={d} M={M}")
