@@ -115,9 +115,10 @@ typedef struct {
 #define TP_F_KERNEL_TC 0x20u      /* force the tcgen05/TMA kernels (rows % 128, K % 64); default:
                                      tcgen05 where supported, except e4m3 weights at decode token counts
                                      (M <= 64).  There a whole block (tp_mlp_forward, tp_proj_forward,
-                                     tp_layer_forward; 128-row tiles, k % 128) runs as one tcgen05 launch
-                                     on hi/lo activation codes (TP_F_FP8_HILO); with this flag that launch
-                                     widens the weights to bf16 instead.  The halves on their own
+                                     tp_layer_forward; 128-row tiles, k % 128) runs as one tcgen05 launch:
+                                     on hi/lo activation codes (TP_F_FP8_HILO) up to 32 tokens, widening
+                                     the weights to bf16 from 33 to 64 (measured faster there); with this
+                                     flag that launch widens the weights at every decode token count.  The halves on their own
                                      (tp_colpar_forward, tp_rowpar_forward, TP_F_SPLIT_BLOCK) go to the
                                      TMA-fed mma.sync kernel (M <= 32, 128-row tiles, k % 128, a workspace
                                      given; widening in registers, work split evenly over two CTAs per SM,
@@ -137,8 +138,8 @@ typedef struct {
                                      into two e4m3 codes (x / s = hi + lo, s a power of two per token:
                                      the token's row of x, or its shard's columns of h / o_in) and
                                      multiplies e4m3 x e4m3, the weights straight from shared memory.
-                                     This is what those blocks run by default (the flag also overrides
-                                     TP_F_KERNEL_TC).  The split is exact for every activation of at
+                                     This is what those blocks run by default up to 32 tokens; the flag
+                                     asks for it up to 64 and overrides TP_F_KERNEL_TC.  The split is exact for every activation of at
                                      least 2^-10 of its token's largest (2^-2 of the scaled range): those
                                      are multiplied as the bf16 values they are.  A smaller activation
                                      loses the bits below 2^-17 of the token's largest, so the result

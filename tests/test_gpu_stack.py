@@ -175,8 +175,10 @@ def test_405b_layer_full_size_decode_batch(dev):
 @pytest.mark.parametrize("M,wtype,fl", [(16, tpx.TP_BF16, 0), (5, tpx.TP_BF16, 0),
                                         (16, tpx.TP_FP8_E4M3, tpx.TP_F_KERNEL_TC),
                                         (16, tpx.TP_FP8_E4M3, tpx.TP_F_FP8_HILO),
-                                        (40, tpx.TP_FP8_E4M3, tpx.TP_F_FP8_HILO)],
-                         ids=["bf16-16", "bf16-5", "fp8-widened-16", "fp8-split-16", "fp8-split-40"])
+                                        (40, tpx.TP_FP8_E4M3, tpx.TP_F_FP8_HILO),
+                                        (40, tpx.TP_FP8_E4M3, 0)],
+                         ids=["bf16-16", "bf16-5", "fp8-widened-16", "fp8-split-16", "fp8-split-40",
+                              "fp8-default-40"])
 def test_layer_norm_folded_into_blocks(dev, M, wtype, fl):
     """Decode layers run as two launches: the RMSNorms become per-token factors on the
     column-parallel accumulators (the attention block computes its input's factors, and its
@@ -195,7 +197,8 @@ def test_layer_norm_folded_into_blocks(dev, M, wtype, fl):
     scratch = torch.empty(tpx.tp_layer_scratch_bytes(lay.sh, M), dtype=torch.uint8, device=dev)
     ws = tpx.new_workspace(lay.sh, M, dev)
     x = inputs.normal_bf16((M, d), 1.0, 4, inputs.STREAM_X, dev)
-    # two block launches; with split activations each block is preceded by the small kernel
+    # two block launches; with split activations each block is preceded by the small kernel (the
+    # default e4m3 block widens the weights above 32 tokens: no small kernel at M = 40)
     # that takes its input's per-token maxima
     n0 = tpx.tp_launch_count()
     y = lay.gpu(x, scratch, ws, fl)
