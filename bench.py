@@ -504,6 +504,8 @@ def run_lm_head(hx, K, W, t_override=0):
 
     ms, launches, clk = hx.timed(K, W, step)
     c = hx.per_call_ms(max(10, K), lambda: tpx.tp_lm_head_forward(wd, w_p, x, logits, ws=ws, stream=hx.stream))
+    # e2e: the token ids in from host memory, the fp32 logits back, every step
+    e2e = hx.e2e(K, W, [(ids, logits)], lambda j: step(), M, "tokens/s")
     head_bytes = 2.0 * d * V + 2.0 * M * d + 4.0 * M * V
     pk = peaks()
     return {"workload": "70b-lm-head-decode", "value": M * K / (ms * 1e-3), "unit": "tokens/s", "steps": K,
@@ -512,7 +514,7 @@ def run_lm_head(hx, K, W, t_override=0):
             "roofline": {"bound": "hbm", "kernel": "tc_kernel (vocabulary-parallel lm_head)",
                          "achieved": head_bytes / (c * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                          "frac": head_bytes / (c * 1e-3) / 1e9 / pk["hbm"], "traffic": None},
-            "gpu_launches": launches, "clocks": clk}
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk}
 
 
 def run_attn(hx, K, W, t_override=0):
@@ -540,6 +542,8 @@ def run_attn(hx, K, W, t_override=0):
     step = lambda: tpx.tp_attn_block_forward(q, q_w, o, o_w, x, x, kc, vc, lens, y, qkv, o_in, bws, stream=hx.stream)
     ms, launches, clk = hx.timed(K, W, step)
     c = hx.per_call_ms(max(10, K), lambda: tpx.tp_attn_decode(sh, qkv, kc, vc, lens, o_in, aws, stream=hx.stream))
+    # e2e: x in from host memory and y back every step (the KV cache stays resident)
+    e2e = hx.e2e(K, W, [(x, y)], lambda j: step(), M, "tokens/s")
     cache_bytes = 2.0 * M * n_kv * L * hd * 2
     w_bytes = 2.0 * ((n_q + 2 * n_kv) * hd * d + n_q * hd * d)
     pk = peaks()
@@ -551,7 +555,7 @@ def run_attn(hx, K, W, t_override=0):
             "roofline": {"bound": "hbm", "kernel": "decode attention (append + attention pass)",
                          "achieved": cache_bytes / (c * 1e-3) / 1e9, "peak": pk["hbm"], "unit": "GB/s",
                          "frac": cache_bytes / (c * 1e-3) / 1e9 / pk["hbm"], "attn_us": 1e3 * c, "traffic": None},
-            "gpu_launches": launches, "clocks": clk}
+            "e2e": e2e, "gpu_launches": launches, "clocks": clk}
 
 
 # ----------------------------------------------------------------------- CPU oracle on the host
@@ -747,7 +751,7 @@ def main():
                "warmup": W, "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": head["dtype"], "data": "synthetic (seeded normals, random-init weights)",
                "config": dict(head["config"], parallelism="replicas" if world > 1 else "single"),
-               "roofline": head["roofline"], "e2e": head["e2e"], "cpu_baseline": head["cpu_baseline"],
+               "roofline": head["roofline"], "e2e": head.get("e2e"), "cpu_baseline": head["cpu_baseline"],
                "gpu_launches": head["gpu_launches"], "clocks": head["clocks"]}
         for k in ("weight_gb", "hbm_gbs_step", "layer_frac", "tflop_per_step", "per_M", "hbm_frac_step"):
             if k in head:
