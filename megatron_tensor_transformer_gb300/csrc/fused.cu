@@ -43,25 +43,28 @@ constexpr int kProducer = 4, kMma = 5;
 constexpr int kSyncItem = 0, kSyncExit = 1, kSyncNormTiles = 2, kSyncInNorm = 3, kSyncDone = 8,
               kSyncTicket = 128;
 
-// bf16 weights: each stage holds one 64-wide k-block, the 128 x 64 bf16 weight tile (128-byte
-// swizzle) the MMA reads from shared memory.  e4m3 weights: each stage holds a 128-wide k-block,
-// the 128 x 128 e4m3 tile as TMA brings it (128-byte swizzle: 128 contiguous bytes per row, as
-// for bf16; 64-byte rows at the weights' row stride read HBM at about half the rate), and two
-// 64-wide activation tiles.  Converter warps widen the tile, exactly, to bf16 in tensor memory
-// (one of kASlots 64-column A slots from column kACol0) and the MMA reads A from there.  A warp
-// may only address one quarter of the TMEM lanes, so the converters come as two warps per
-// quarter, each widening one 64-wide half of its 32 rows.  With e4m3 weights the activation
-// tiles travel in a ring of their own (kSB slots, issued by a second producer warp and freed
-// by the MMA), so a weight stage is free again as soon as the converters have read it: the
-// weight ring is then almost entirely in flight from HBM.
-// Split activations (e4m3 weights): the weight tile goes to the MMA as it is, and four
-// converter warps split each activation tile, in place, into the e4m3 tiles hi and lo (rows 0..BN-1
-// and BN..2BN-1 of the same bytes); the MMA multiplies e4m3 x e4m3 with N = 2 BN, and the
-// epilogue adds the two column halves before the scales.
-// Split activations take two 128-wide k-blocks per stage (kSub): the MMA-issuing thread pays a
-// fixed cost per stage (two mbarrier waits and two commits besides the MMAs; measured alone, about
-// 270 ns for one 16 KB k-block), which capped the block at one k-block per 425 ns per SM; per
-// 32 KB stage the same cost covers twice the bytes.
+// A pipeline stage holds kSub k-blocks of weights, brought by one TMA copy (the weights viewed as
+// {k within a k-block, row, k-block, shard}), and their activation tiles, brought by one more
+// (the activations viewed as {64 columns, token, 64-column chunk}).  Each SM completes TMA copies
+// at a nearly fixed rate per copy, so fewer, larger copies stream faster.
+// bf16 weights: two 64-wide k-blocks per stage, the 128 x 64 bf16 weight tiles (128-byte swizzle)
+// the MMA reads from shared memory, with their activation tiles in the same stage.
+// e4m3 weights, hi/lo activation codes (SPLIT): two 128-wide k-blocks per stage, the 128 x 128
+// e4m3 tiles as TMA brings them (128-byte swizzle: 128 contiguous bytes per row; 64-byte rows at
+// the weights' row stride read HBM at about half the rate) go to the MMA as they are.  The
+// activation tiles travel in a ring of their own (kSB slots, a second producer warp), and four
+// converter warps split each in place into the e4m3 tiles hi and lo (rows 0..BN-1 and BN..2BN-1
+// of the same bytes); the MMA multiplies e4m3 x e4m3 with N = 2 BN and the epilogue adds the two
+// column halves before the scales.  One MMA commit per stage frees the weight stage, and the
+// activation producer learns from the same barrier that the slot is free.
+// e4m3 weights, widened (TP_F_KERNEL_TC, and above 32 tokens): one 128-wide k-block per stage;
+// converter warps widen the tile, exactly, to bf16 in tensor memory (one of kASlots 64-column A
+// slots from column kACol0) and the MMA reads A from there.  A warp may only address one quarter
+// of the TMEM lanes, so the converters come as two warps per quarter, each widening one 64-wide
+// half of its 32 rows; a weight stage is free again as soon as they have read it.
+// Two k-blocks per stage: the MMA-issuing thread pays a fixed cost per stage (its barrier waits
+// and commits; measured alone, about 270 ns for one 16 KB k-block), which capped an SM at one
+// k-block per 425 ns; a 32 KB stage spreads it over twice the bytes.
 template <int BN, bool FP8, bool SPLIT = false>
 struct FCfg {
   static constexpr int kKB = FP8 ? 2 * FBK : FBK;        // k per k-block
