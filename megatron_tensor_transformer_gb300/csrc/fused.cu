@@ -13,16 +13,18 @@
 //
 // Items are taken in that order from one atomic counter (each CTA's first item is its
 // block index, so its weights start streaming before the previous kernel has finished).
-// A stage-2 item of shard s needs the whole stage-1 output of shard s: its producer issues
-// the weight tiles ahead, then waits (bounded) until shard s's stage-1 count is complete.
+// A stage-2 item of shard s needs the whole stage-1 output of shard s: its weight tiles are
+// issued ahead, and its activation tiles once shard s's stage-1 count is complete (a bounded
+// wait).
 // The last of the t shard items of a row tile (ticket) folds the t partials in shard
 // order, adds the residual and writes y: the same left fold, bit for bit, as the separate
 // fold kernel.  No CTA idles while another finishes a second wave of one kernel, and no
 // launch gap separates the halves or the fold.
 //
-// Warp roles per CTA (one CTA per SM): warps 0-3 epilogue, warp 4 TMA producer (and the
-// scheduler), warp 5 MMA issuer.  Every wait is bounded in time; on expiry the kernel
-// records the device error word, drains, frees its TMEM and returns.
+// Warp roles per CTA (one CTA per SM): warps 0-3 epilogue, warp 4 weight producer (and the
+// scheduler), warp 5 MMA issuer; with e4m3 weights, converter warps from warp 6 and then the
+// activation producer.  Every wait is bounded in time; on expiry the kernel records the
+// device error word, drains, frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
